@@ -1,0 +1,21 @@
+"""TriAttention periodic KV-cache compression step on B300 (sm_103a).
+
+The compute path is libtri.so (CUDA kernels behind the C ABI in include/tri.h);
+`tri` is its ctypes binding.  There is no CPU fallback.
+"""
+from .tri import (  # noqa: F401
+    KVCache,
+    Params,
+    Stats,
+    TriError,
+    tri_calibrate_stats,
+    tri_clear_device_status,
+    tri_compact_kv,
+    tri_compress_step,
+    tri_get_device_status,
+    tri_score,
+    tri_select_topb,
+    tri_version,
+    tri_workspace_bytes,
+    workspace,
+)

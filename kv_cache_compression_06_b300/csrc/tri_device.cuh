@@ -1,0 +1,170 @@
+// Device helpers shared by every libtri kernel: inline-PTX wrappers for
+// mbarriers, bulk (TMA) copies and cp.async, bounded waits, the device status
+// word, block-wide reductions and scans, and the order-preserving float key.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/tri.h"
+
+namespace tri {
+
+constexpr int kThreads = 256;                   // CTA size of the score / fused kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kStageBytes = 16384;              // one pipeline stage (K tile or K+V chunk)
+constexpr int kStages = 4;
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kTileKeys = 2048;                 // keys per CTA in the split (long-unit) path
+constexpr int kSelThreads = 512;                // CTA size of the select/compact kernel
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // bounded device waits: 2 s
+
+// First device-side error since the last clear (0 = TRI_OK).
+__device__ int g_tri_status = 0;
+
+__device__ __forceinline__ void set_status(int code) { atomicCAS(&g_tri_status, 0, code); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with `parity` to complete.  Gives up after kWaitLimitNs,
+// records TRI_ERR_TIMEOUT and returns false (the caller then leaves the CTA).
+__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      set_status(TRI_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- bulk copy (TMA, untiled)
+// global -> shared, completion counted in bytes on `bar`.  Both addresses 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- cp.async (16 B)
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- arithmetic
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Order-preserving map of an fp32 score to u32 (larger float -> larger key);
+// NaN maps to 0 (ranks lowest), -0 and +0 map to the same key.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  if (f != f) return 0u;
+  uint32_t u = __float_as_uint(f);
+  if (f == 0.0f) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------- block reductions
+template <int G>
+__device__ __forceinline__ void block_sum(float (&v)[G], float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float x = v[h];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    v[h] = x;
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) red[warp * G + h] = v[h];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float t = 0.f;
+    for (int w = 0; w < nw; ++w) t += red[w * G + h];
+    v[h] = t;
+  }
+  __syncthreads();
+}
+
+// Exclusive prefix sum of one int per thread across the CTA; *total receives
+// the CTA-wide sum.  sm needs 32 ints.
+__device__ __forceinline__ int block_excl_scan(int v, int *sm, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? sm[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sm[lane] = w;
+  }
+  __syncthreads();
+  const int base = warp ? sm[warp - 1] : 0;
+  *total = sm[nw - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+}  // namespace tri
