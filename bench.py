@@ -1,0 +1,343 @@
+"""Benchmark of the TriAttention compression step on the Qwen3-8B-shaped full
+step (36 layers x 8 KV heads x 32 query heads, d=128, bf16, 16 sequences of
+N=2176 keys, budget B=2048, offsets 2^0..2^16).
+
+One step = one call of tri_compress_step over the whole batch (score every key,
+GQA z/max, top-B, in-place compaction of K and V), with inputs resident in HBM.
+The compaction is in place, so the cache is restored from a pristine copy
+before every step (untimed; the 5.1 GB copy also flushes the 126 MB L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle on a
+bounded sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+# The CPU-oracle leg runs single-threaded: pin numpy's BLAS pool before import.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "cached keys scored+selected+compacted/sec"
+WORKLOAD = "qwen3_8b_36l_b16_n2176"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def _config(w, extra=None):
+    c = {"workload": w.name, "layers": w.L, "kv_heads": w.Hkv, "q_heads": w.Hq, "head_dim": w.d,
+         "dtype_cache": w.dtype, "batch": w.S, "n_keys": w.n_keys, "budget": w.budget,
+         "offsets": f"2^0..2^{int(math.log2(max(w.offsets)))}", "theta": w.theta}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_sample(w, budget_s, max_units=None, seed=0):
+    """Runs the fp64 oracle on sampled units of layer 0 (generated on the CPU)
+    until budget_s seconds of CPU work; returns (keys, seconds, units, threads)."""
+    from oracle import tri_oracle as O
+    from synth import generate_layer
+
+    lay = generate_layer(w, 0, "cpu", with_q=True)
+    stats = O.calibrate(lay["q_pre"].double().numpy(), w.pairing)
+    rng = np.random.default_rng(seed)
+    keys = units = 0
+    t0 = time.perf_counter()
+    while True:
+        s, g = int(rng.integers(w.S)), int(rng.integers(w.Hkv))
+        n = lay["seq_len"][s]
+        kr = lay["k"][s, g, :n].double().numpy()
+        vr = lay["v"][s, g, :n].double().numpy()
+        sl = slice(g * w.G, (g + 1) * w.G)
+        O.compress_unit(stats[0][sl], stats[1][sl], stats[2][sl], kr, vr, np.arange(n, dtype=np.float64),
+                        n, list(w.offsets), w.theta, w.budget, w.pairing)
+        keys += n
+        units += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_units and units >= max_units):
+            return keys, el, units, 1
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = []
+    total_keys = 0
+    for i in range(args.warmup + args.steps):
+        keys, el, units, cores = oracle_sample(w, 0.0, max_units=2, seed=1000 + i)
+        if i >= args.warmup:
+            per_step.append(el)
+            total_keys += keys
+    T = sum(per_step)
+    value = total_keys / T
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * T / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(w, {"sample": "2 units (seq, KV head) of layer 0 per step"}),
+            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": cores, "kind": "oracle",
+                             "sample": "per step: 2 random units of layer 0 (N=2176 keys each), "
+                                       "per-offset route, fp64 numpy, 1 thread"},
+            "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ traffic record
+def _traffic_record(kernel_src_hash):
+    """Per-launch DRAM bytes of the fused kernel from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+        if rec.get("kernel_src_sha1") == kernel_src_hash and rec.get("workload") == WORKLOAD:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def kernel_src_hash():
+    import hashlib
+    h = hashlib.sha1()
+    for f in ("tri.cu", "tri_path.cuh", "tri_device.cuh"):
+        with open(os.path.join(ROOT, "kv_cache_compression_06_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+# ------------------------------------------------------------------ GPU leg
+def run_b300(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import kv_cache_compression_06_b300 as tk
+    from synth import generate
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    # CPU oracle baseline first (rank 0, N=1), before any GPU work.
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        keys, el, units, cores = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": keys / el, "unit": "keys/s", "cores": cores, "kind": "oracle",
+               "sample": f"{units} random units (seq, KV head) of layer 0, N=2176 keys each, "
+                         f"{el:.1f} s; per-offset route, fp64 numpy, 1 thread"}
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    data = generate(w, device=dev)
+    cache = tk.KVCache(data["k"], data["v"], data["seq_len"], Hkv=w.Hkv)
+    stats = tk.tri_calibrate_stats(data["q_pre"])
+    del data["q_pre"]
+    params = tk.Params(w.theta, data["t"], w.offsets, w.budget)
+    ws = tk.workspace(cache, stats, params)
+    launches = 1 if ws is None else 2
+    k0, v0 = cache.k.clone(), cache.v.clone()
+    idx = torch.empty((w.L, w.S, w.Hkv, w.budget), dtype=torch.int32, device=dev)
+    new_len = torch.empty(w.S, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def restore():
+        cache.k.copy_(k0)
+        cache.v.copy_(v0)
+
+    def step():
+        tk.tri_compress_step(cache, stats, params, idx_out=idx, new_len=new_len, ws=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        restore()
+        step()
+    torch.cuda.synchronize()
+    assert tk.tri_get_device_status() == 0
+
+    # algorithmic bytes: K read for scoring + K/V moved (read + write) by compaction
+    B, rb = w.budget, w.d * w.esize
+    ii = idx.view(-1, B).long()
+    ar = torch.arange(B, device=dev)
+    e0 = torch.where((ii != ar).any(dim=1), (ii != ar).int().argmax(dim=1), torch.full_like(ii[:, 0], B))
+    M = int((B - e0).clamp_min(0).sum())
+    units = w.L * w.S * w.Hkv
+    n_keys = units * w.n_keys
+    alg_bytes = n_keys * rb + 4 * M * rb
+    alg_bytes_full_move = n_keys * rb + 4 * units * B * rb
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        torch.cuda.nvtx.range_push("timed")
+        for i in range(args.steps):
+            restore()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+    if world > 1:
+        dist.barrier()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    t_step = sum(ms) / len(ms) / 1e3
+    if world > 1:
+        tt = torch.tensor([t_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt)
+    assert tk.tri_get_device_status() == 0
+
+    # end to end through the public API from pinned host buffers
+    hk = torch.empty_like(k0, device="cpu").pin_memory()
+    hv = torch.empty_like(v0, device="cpu").pin_memory()
+    hk.copy_(k0)
+    hv.copy_(v0)
+    ok_ = torch.empty_like(hk).pin_memory()
+    ov = torch.empty_like(hv).pin_memory()
+    oi = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
+    on = torch.empty(new_len.shape, dtype=torch.int32).pin_memory()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        cache.k.copy_(hk, non_blocking=True)
+        cache.v.copy_(hv, non_blocking=True)
+        step()
+        ok_.copy_(cache.k, non_blocking=True)
+        ov.copy_(cache.v, non_blocking=True)
+        oi.copy_(idx, non_blocking=True)
+        on.copy_(new_len, non_blocking=True)
+    torch.cuda.synchronize()
+    t_e2e = (time.perf_counter() - t0) / e2e_steps
+    h2d = hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
+    d2h = h2d + oi.numel() * 4 + on.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = _peaks()
+    achieved = alg_bytes / t_step / 1e9
+    line = {
+        "metric": METRIC, "value": world * n_keys / t_step, "unit": "keys/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": _config(w, {"l2": f"cache restored from a pristine {2 * k0.numel() * 2 / 1e9:.1f} GB copy "
+                                    "before every step (flushes L2; untimed)", "parallelism": f"replicas x{world}"}),
+        "compress_step_us": t_step * 1e6,
+        "hbm_gbs": achieved,
+        "hbm_frac_of_8tbs": achieved / 8000.0,
+        "moved_rows": M, "moved_rows_if_all_B": units * B,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": _traffic_record(kernel_src_hash()),
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "algorithmic_bytes_if_all_B_moved": alg_bytes_full_move,
+                     "kernel": "fused_kernel<128,4,bf16>" if launches == 1 else "score_tiles+select_compact"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * n_keys / t_e2e, "unit": "keys/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "clocks": clk.summary(),
+        "gpu_launches": launches * args.steps,
+        "step_ms_min": min(ms), "step_ms_median": float(np.median(ms)),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="use only the first N layers (small case for ncu captures; default: all 36)")
+    args = ap.parse_args()
+    from synth import WORKLOADS
+    w = WORKLOADS[WORKLOAD]
+    if args.layers:
+        w = w.with_(L=args.layers)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_b300(args, w)
+
+
+if __name__ == "__main__":
+    main()
