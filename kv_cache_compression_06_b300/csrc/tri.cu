@@ -93,18 +93,22 @@ struct FusedArgs {
   StepConst sc;
 };
 
+// Shared-memory layout of the fused kernel.  Scores of head h live at
+// scores[h * sstride + i]; sstride = capp + 4 (= 4 mod 32) keeps the per-row
+// score writes of the different heads in different banks.
 struct FusedLayout {
-  int bars, wts, red, hist, sm, scores, idx, total;
+  int bars, wts, red, hist, sm, scores, idx, sstride, total;
   __host__ __device__ FusedLayout(int G, int F, int capp) {
+    sstride = capp + 4;
     int o = kRingBytes;
-    bars = o;   o += 128;
+    bars = o;   o += 128;                 // kStages score barriers + kStages compaction barriers
     wts = o;    o += align_up(G * 3 * F * 4, 128);
     red = o;    o += 256;
     hist = o;   o += 1024;
     sm = o;     o += 256;
-    scores = o; o += align_up(G * capp * 4, 128);
+    scores = o; o += align_up(G * sstride * 4, 128);
     if (G >= 2) {
-      idx = scores + capp * 4;   // overlays head 1's scores (dead after z/max)
+      idx = scores + sstride * 4;   // overlays head 1's scores (dead after z/max)
     } else {
       idx = o;
       o += align_up(capp * 4, 128);
@@ -150,24 +154,26 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1)) fused_kernel(const
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
+  const int ss = lay.sstride;
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 32);
+    for (int st = 0; st < kStages; ++st) mbar_init(&bars[kStages + st], 1);
     fence_mbar_init();
   }
   build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc);
   __syncthreads();
   LaneWeights<G> lw;
   load_lane_weights<G, F>(lw, wts, (tid & 31) % RowGeom<D, BF16>::LPR);
-  if (!score_unit_rows<D, G, BF16>(c, l, s, g, 0, N, ring, bars, scores, a.capp, lw, a.inter != 0))
+  if (!score_unit_rows<D, G, BF16>(c, l, s, g, 0, N, ring, bars, scores, ss, lw, a.inter != 0))
     return;
 
   float mu[G], inv[G];
-  head_moments<G>(scores, a.capp, N, red, mu, inv);
+  head_moments<G>(scores, ss, N, red, mu, inv);
   uint32_t *keys = reinterpret_cast<uint32_t *>(scores);   // overlays head 0's scores
   for (int i = tid; i < N; i += nt) {
     float sv[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) sv[h] = scores[h * a.capp + i];
+    for (int h = 0; h < G; ++h) sv[h] = scores[h * ss + i];
     float z = (sv[0] - mu[0]) * inv[0];
 #pragma unroll
     for (int h = 1; h < G; ++h) z = fmaxf(z, (sv[h] - mu[h]) * inv[h]);
@@ -188,7 +194,10 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1)) fused_kernel(const
   const int e0 = build_kept(keys, N, B, T, ntie, idxs, sm);
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
-  compact_unit(c, l, s, g, idxs, e0, B, N, ring);
+  // The ring was last read by generic loads (scoring); TMA writes it next.
+  fence_proxy_async_smem();
+  __syncthreads();
+  if ((tid >> 5) == 0) compact_unit_tma(c, l, s, g, idxs, e0, B, N, ring, bars + kStages);
 }
 
 // ---------------------------------------------------------------- long units: tiles
@@ -203,6 +212,8 @@ struct TileArgs {
   StepConst sc;
 };
 
+constexpr int kTileStride = kTileKeys + 4;   // per-head score stride (= 4 mod 32: no bank conflicts)
+
 struct TileLayout {
   int bars, wts, red, scores, total;
   __host__ __device__ TileLayout(int G, int F) {
@@ -210,7 +221,7 @@ struct TileLayout {
     bars = o;   o += 128;
     wts = o;    o += align_up(G * 3 * F * 4, 128);
     red = o;    o += 256;
-    scores = o; o += G * kTileKeys * 4;
+    scores = o; o += G * kTileStride * 4;
     total = o;
   }
 };
@@ -278,15 +289,15 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1)) score_tiles_kernel
   __syncthreads();
   LaneWeights<G> lw;
   load_lane_weights<G, F>(lw, wts, (tid & 31) % RowGeom<D, BF16>::LPR);
-  if (!score_unit_rows<D, G, BF16>(c, l, s, g, i0, n, ring, bars, scores, kTileKeys, lw,
+  if (!score_unit_rows<D, G, BF16>(c, l, s, g, i0, n, ring, bars, scores, kTileStride, lw,
                                    a.inter != 0))
     return;
   for (int i = tid; i < n; i += nt) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * c.cap + i0 + i] = scores[h * kTileKeys + i];
+    for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * c.cap + i0 + i] = scores[h * kTileStride + i];
   }
   float mu[G], m2[G];
-  head_mean_m2<G>(scores, kTileKeys, n, red, mu, m2);
+  head_mean_m2<G>(scores, kTileStride, n, red, mu, m2);
   if (tid == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h)
@@ -364,9 +375,10 @@ struct SCArgs {
 };
 
 struct SCLayout {
-  int hist, sm, mom, keys, idx, total;
+  int bars, hist, sm, mom, keys, idx, total;
   __host__ __device__ SCLayout(int capp, int bcap) {
     int o = kRingBytes;
+    bars = o; o += 128;
     hist = o; o += 1024;
     sm = o;   o += 256;
     mom = o;  o += 128;
@@ -380,6 +392,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const SC
   extern __shared__ __align__(1024) char smem[];
   const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap);
   char *ring = smem;
+  uint64_t *cbars = reinterpret_cast<uint64_t *>(smem + lay.bars);
   uint32_t *hist = reinterpret_cast<uint32_t *>(smem + lay.hist);
   int *sm = reinterpret_cast<int *>(smem + lay.sm);
   float *mom = reinterpret_cast<float *>(smem + lay.mom);
@@ -405,6 +418,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const SC
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(&cbars[st], 1);
+    fence_mbar_init();
+  }
   if (a.mode == 2) {
     const int *src = a.idx_in + (long long)u * B;
     int bad = 0;
@@ -423,7 +440,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const SC
     __syncthreads();
     const int e0 = sm[36];
     __syncthreads();
-    compact_unit(c, l, s, g, idxs, e0, B, N, ring);
+    if ((tid >> 5) == 0) compact_unit_tma(c, l, s, g, idxs, e0, B, N, ring, cbars);
     return;
   }
   if (a.mode == 0) {
@@ -446,7 +463,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const SC
   const int e0 = build_kept(keys, N, B, T, ntie, idxs, sm);
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
-  if (a.mode == 0) compact_unit(c, l, s, g, idxs, e0, B, N, ring);
+  if (a.mode == 0) {
+    __syncthreads();
+    if ((tid >> 5) == 0) compact_unit_tma(c, l, s, g, idxs, e0, B, N, ring, cbars);
+  }
 }
 
 // ================================================================ host side

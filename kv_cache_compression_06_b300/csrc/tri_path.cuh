@@ -94,35 +94,51 @@ struct RowGeom {
   static constexpr int RB = D * ES;
 };
 
-// Loads the 4 bands (re, im) of this lane from a row in shared memory.
+// The 4 bands a lane owns, as packed pairs: re01 = (re_0, re_1), re23, im01, im23.
+struct LaneBands {
+  uint64_t re01, re23, im01, im23;
+};
+
+// Loads the 4 bands of this lane (bands 4j..4j+3) from a row in shared memory.
 template <int D, bool BF16>
-__device__ __forceinline__ void load_bands(const char *row, int j, bool inter, float (&re)[4],
-                                           float (&im)[4]) {
+__device__ __forceinline__ LaneBands load_bands(const char *row, int j, bool inter) {
   constexpr int F = D / 2;
+  LaneBands x;
   if constexpr (BF16) {
     if (!inter) {
+      // rotate-half: re = elements 4j..4j+3, im = elements F+4j..F+4j+3
       const uint2 lo = *reinterpret_cast<const uint2 *>(row + 2 * (4 * j));
       const uint2 hi = *reinterpret_cast<const uint2 *>(row + 2 * (F + 4 * j));
-      re[0] = bf16lo(lo.x); re[1] = bf16hi(lo.x); re[2] = bf16lo(lo.y); re[3] = bf16hi(lo.y);
-      im[0] = bf16lo(hi.x); im[1] = bf16hi(hi.x); im[2] = bf16lo(hi.y); im[3] = bf16hi(hi.y);
+      x.re01 = pk(bf16lo(lo.x), bf16hi(lo.x));
+      x.re23 = pk(bf16lo(lo.y), bf16hi(lo.y));
+      x.im01 = pk(bf16lo(hi.x), bf16hi(hi.x));
+      x.im23 = pk(bf16lo(hi.y), bf16hi(hi.y));
     } else {
+      // interleaved: band b = elements (2b, 2b+1) -> one 32-bit word per band
       const uint4 w = *reinterpret_cast<const uint4 *>(row + 2 * (8 * j));
-      re[0] = bf16lo(w.x); im[0] = bf16hi(w.x); re[1] = bf16lo(w.y); im[1] = bf16hi(w.y);
-      re[2] = bf16lo(w.z); im[2] = bf16hi(w.z); re[3] = bf16lo(w.w); im[3] = bf16hi(w.w);
+      x.re01 = pk(bf16lo(w.x), bf16lo(w.y));
+      x.re23 = pk(bf16lo(w.z), bf16lo(w.w));
+      x.im01 = pk(bf16hi(w.x), bf16hi(w.y));
+      x.im23 = pk(bf16hi(w.z), bf16hi(w.w));
     }
   } else {
     if (!inter) {
       const float4 lo = *reinterpret_cast<const float4 *>(row + 4 * (4 * j));
       const float4 hi = *reinterpret_cast<const float4 *>(row + 4 * (F + 4 * j));
-      re[0] = lo.x; re[1] = lo.y; re[2] = lo.z; re[3] = lo.w;
-      im[0] = hi.x; im[1] = hi.y; im[2] = hi.z; im[3] = hi.w;
+      x.re01 = pk(lo.x, lo.y);
+      x.re23 = pk(lo.z, lo.w);
+      x.im01 = pk(hi.x, hi.y);
+      x.im23 = pk(hi.z, hi.w);
     } else {
       const float4 a = *reinterpret_cast<const float4 *>(row + 4 * (8 * j));
       const float4 b = *reinterpret_cast<const float4 *>(row + 4 * (8 * j + 4));
-      re[0] = a.x; im[0] = a.y; re[1] = a.z; im[1] = a.w;
-      re[2] = b.x; im[2] = b.y; re[3] = b.z; im[3] = b.w;
+      x.re01 = pk(a.x, a.z);
+      x.re23 = pk(b.x, b.z);
+      x.im01 = pk(a.y, a.w);
+      x.im23 = pk(b.y, b.w);
     }
   }
+  return x;
 }
 
 // Sums v[0..G) across the LPR lanes of a row group.  The first log2(G) levels
@@ -149,24 +165,32 @@ __device__ __forceinline__ float group_reduce(float (&v)[G], int lane) {
   return x;
 }
 
-// Lane-private weights of the 4 bands a lane owns, for each of the G heads.
+// Lane-private weights of the 4 bands a lane owns, for each of the G heads, as
+// packed pairs over bands (4j, 4j+1) and (4j+2, 4j+3).
 template <int G>
 struct LaneWeights {
-  float4 ar[G], ai[G], w[G];
+  uint64_t ar01[G], ar23[G], ai01[G], ai23[G], w01[G], w23[G];
 };
 
 template <int G, int F>
 __device__ __forceinline__ void load_lane_weights(LaneWeights<G> &lw, const float *wts, int j) {
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    lw.ar[h] = *reinterpret_cast<const float4 *>(wts + (h * 3 + 0) * F + 4 * j);
-    lw.ai[h] = *reinterpret_cast<const float4 *>(wts + (h * 3 + 1) * F + 4 * j);
-    lw.w[h] = *reinterpret_cast<const float4 *>(wts + (h * 3 + 2) * F + 4 * j);
+    const float4 ar = *reinterpret_cast<const float4 *>(wts + (h * 3 + 0) * F + 4 * j);
+    const float4 ai = *reinterpret_cast<const float4 *>(wts + (h * 3 + 1) * F + 4 * j);
+    const float4 w = *reinterpret_cast<const float4 *>(wts + (h * 3 + 2) * F + 4 * j);
+    lw.ar01[h] = pk(ar.x, ar.y);
+    lw.ar23[h] = pk(ar.z, ar.w);
+    lw.ai01[h] = pk(ai.x, ai.y);
+    lw.ai23[h] = pk(ai.z, ai.w);
+    lw.w01[h] = pk(w.x, w.y);
+    lw.w23[h] = pk(w.z, w.w);
   }
 }
 
 // Scores the rows [0, nrows) of a tile in shared memory; s_{h, row0 + r} goes to
-// scores[h * sstride + row0 + r].
+// scores[h * sstride + row0 + r].  Per lane and head: 6 paired FMAs over its 4
+// bands (Re A * Re k~ + Im A * Im k~ + W * |k~|), then a cross-lane sum.
 template <int D, int G, bool BF16>
 __device__ __forceinline__ void score_tile(const char *tile, int nrows, int row0, float *scores,
                                            int sstride, const LaneWeights<G> &lw, bool inter) {
@@ -180,32 +204,32 @@ __device__ __forceinline__ void score_tile(const char *tile, int nrows, int row0
   for (int rb = 0; rb < nrows; rb += nw * RPW) {
     const int r = rb + warp * RPW + rsub;
     const bool valid = r < nrows;
-    float re[4], im[4];
+    LaneBands x;
     if (valid) {
-      load_bands<D, BF16>(tile + (long long)r * RB, j, inter, re, im);
+      x = load_bands<D, BF16>(tile + (long long)r * RB, j, inter);
     } else {
-#pragma unroll
-      for (int b = 0; b < 4; ++b) re[b] = im[b] = 0.f;
+      x.re01 = x.re23 = x.im01 = x.im23 = 0ull;
     }
-    float mg[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) mg[b] = sqrt_approx(fmaf(re[b], re[b], im[b] * im[b]));
+    uint64_t mg01, mg23;
+    {
+      float a, b, c, e;
+      upk(ffma2(x.im01, x.im01, fmul2(x.re01, x.re01)), a, b);
+      upk(ffma2(x.im23, x.im23, fmul2(x.re23, x.re23)), c, e);
+      mg01 = pk(sqrt_approx(a), sqrt_approx(b));
+      mg23 = pk(sqrt_approx(c), sqrt_approx(e));
+    }
     float acc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float x = lw.ar[h].x * re[0];
-      x = fmaf(lw.ar[h].y, re[1], x);
-      x = fmaf(lw.ar[h].z, re[2], x);
-      x = fmaf(lw.ar[h].w, re[3], x);
-      x = fmaf(lw.ai[h].x, im[0], x);
-      x = fmaf(lw.ai[h].y, im[1], x);
-      x = fmaf(lw.ai[h].z, im[2], x);
-      x = fmaf(lw.ai[h].w, im[3], x);
-      x = fmaf(lw.w[h].x, mg[0], x);
-      x = fmaf(lw.w[h].y, mg[1], x);
-      x = fmaf(lw.w[h].z, mg[2], x);
-      x = fmaf(lw.w[h].w, mg[3], x);
-      acc[h] = x;
+      uint64_t t = fmul2(lw.ar01[h], x.re01);
+      t = ffma2(lw.ar23[h], x.re23, t);
+      t = ffma2(lw.ai01[h], x.im01, t);
+      t = ffma2(lw.ai23[h], x.im23, t);
+      t = ffma2(lw.w01[h], mg01, t);
+      t = ffma2(lw.w23[h], mg23, t);
+      float lo, hi;
+      upk(t, lo, hi);
+      acc[h] = lo + hi;
     }
     const float s = group_reduce<G, LPR>(acc, lane);
     if (valid && writer) scores[head * sstride + row0 + r] = s;
@@ -401,63 +425,100 @@ __device__ __noinline__ int build_kept(const uint32_t *keys, int n, int K, uint3
 
 // ---------------------------------------------------------------- compaction (a5)
 // In-place ordered gather of K and V rows of unit (l, s, g): row j <- row idx[j]
-// for j in [e0, B) (rows below e0 are kept in place).  Destination chunks are
-// processed in ascending order through a cp.async ring; every load of a chunk
-// completes (wait_group + barrier) before any store of that chunk, and a load of
-// a later chunk only reads slots >= that chunk's first destination, which no
-// earlier store touches, because idx is strictly increasing (idx_j >= j).
-__device__ __noinline__ void compact_unit(const CacheView &c, int l, int s, int g, const int *idx,
-                                          int e0, int B, int N, char *ring) {
+// for j in [e0, B) (rows below e0 are kept in place), executed by warp 0 alone
+// with bulk (TMA) copies; the other warps may leave.
+//
+// Destination chunks of up to 32 rows (K and V, one ring stage) are processed in
+// ascending order.  Lane r of warp 0 owns destination row j0 + r of a chunk.
+// Loads: dense caches copy each run of consecutive source slots with one bulk
+// copy per tensor; paged caches copy row by row.  Stores: one bulk store per
+// tensor for a dense chunk (its destination rows are contiguous), row by row for
+// paged.  In-place safety: a chunk is stored only after its loads completed,
+// and every load of a later chunk reads slots >= that chunk's first destination,
+// which no earlier store touches, since idx is strictly increasing (idx_j >= j).
+// A ring stage is refilled only after the bulk stores that read it finished
+// reading (per-lane bulk async-groups, one group per chunk per lane).
+//
+// cbars: kStages mbarriers initialised with arrival count 1.  Returns false if a
+// wait timed out (status recorded).
+__device__ __noinline__ bool compact_unit_tma(const CacheView &c, int l, int s, int g,
+                                              const int *idx, int e0, int B, int N, char *ring,
+                                              uint64_t *cbars) {
+  const int lane = threadIdx.x & 31;
   const int rb = c.rb;
-  const int pr = rb >> 4;                          // 16-byte pieces per row
-  const int ch = kStageBytes / (2 * rb);           // rows per chunk (K and V)
-  const int per = ch * pr;                         // pieces per tensor per chunk
+  const int ch = min(32, kStageBytes / (2 * rb));   // rows per chunk
   const int M = B - e0;
-  if (M <= 0) return;
+  if (M <= 0) return true;
   const int nch = (M + ch - 1) / ch;
-  const int tid = threadIdx.x, nt = blockDim.x;
-  auto issue = [&](int cidx) {
-    if (cidx < nch) {
-      char *st = ring + (cidx % kStages) * kStageBytes;
-      const int j0 = e0 + cidx * ch;
-      for (int q = tid; q < 2 * per; q += nt) {
-        const int tsr = q >= per;
-        const int rem = q - tsr * per;
-        const int r = rem / pr, p = rem - r * pr;
-        const int j = j0 + r;
-        if (j < B) {
-          const int src = idx[j];
-          const long long off = (src >= 0 && src < N) ? c.row_off(l, s, g, src) : -1;
-          if (off >= 0) cp_async16(st + (long long)q * 16, (tsr ? c.v : c.k) + off + p * 16);
-        }
-      }
-    }
-    cp_async_commit();
-  };
-#pragma unroll 1
-  for (int x = 0; x < kStages - 1; ++x) issue(x);
-#pragma unroll 1
-  for (int cidx = 0; cidx < nch; ++cidx) {
-    issue(cidx + kStages - 1);
-    cp_async_wait<kStages - 1>();
-    __syncthreads();
-    const char *st = ring + (cidx % kStages) * kStageBytes;
+  const bool paged = c.paged();
+
+  auto issue_loads = [&](int cidx) {
+    const int st = cidx % kStages;
+    char *sk = ring + st * kStageBytes;   // K rows [0, ch), then V rows [ch, 2ch)
     const int j0 = e0 + cidx * ch;
-    for (int q = tid; q < 2 * per; q += nt) {
-      const int tsr = q >= per;
-      const int rem = q - tsr * per;
-      const int r = rem / pr, p = rem - r * pr;
-      const int j = j0 + r;
-      if (j < B) {
-        const long long off = c.row_off(l, s, g, j);
-        if (off >= 0)
-          *reinterpret_cast<uint4 *>((tsr ? c.v : c.k) + off + p * 16) =
-              *reinterpret_cast<const uint4 *>(st + (long long)q * 16);
+    const int rows = min(ch, B - j0);
+    int src = -1;
+    bool valid = lane < rows;
+    if (valid) {
+      src = idx[j0 + lane];
+      if (src < 0 || src >= N) {
+        set_status(TRI_ERR_BOUNDS);
+        valid = false;
       }
     }
+    long long off = valid ? c.row_off(l, s, g, src) : -1;
+    if (off < 0) valid = false;
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    if (lane == 0) mbar_arrive_expect_tx(&cbars[st], (uint32_t)__popc(vmask) * 2u * (uint32_t)rb);
+    __syncwarp();
+    if (!paged) {
+      const int prev = __shfl_up_sync(0xffffffffu, src, 1);
+      const bool boundary = !valid || lane == 0 || prev + 1 != src;
+      const unsigned bmask = __ballot_sync(0xffffffffu, boundary);
+      if (valid && boundary) {
+        const unsigned later = (lane == 31) ? 0u : (bmask & (0xffffffffu << (lane + 1)));
+        const int end = later ? (__ffs(later) - 1) : rows;
+        const uint32_t bytes = (uint32_t)(end - lane) * (uint32_t)rb;
+        bulk_g2s(sk + (long long)lane * rb, c.k + off, bytes, &cbars[st]);
+        bulk_g2s(sk + (long long)(ch + lane) * rb, c.v + off, bytes, &cbars[st]);
+      }
+    } else if (valid) {
+      bulk_g2s(sk + (long long)lane * rb, c.k + off, (uint32_t)rb, &cbars[st]);
+      bulk_g2s(sk + (long long)(ch + lane) * rb, c.v + off, (uint32_t)rb, &cbars[st]);
+    }
+  };
+
+  for (int x = 0; x < kStages - 1 && x < nch; ++x) issue_loads(x);
+  bool ok = true;
+  for (int cidx = 0; cidx < nch; ++cidx) {
+    const int st = cidx % kStages;
+    const char *sk = ring + st * kStageBytes;
+    const int j0 = e0 + cidx * ch;
+    const int rows = min(ch, B - j0);
+    if (!mbar_wait(&cbars[st], (uint32_t)((cidx / kStages) & 1))) {
+      ok = false;
+      break;
+    }
+    if (!paged) {
+      if (lane == 0) {
+        const long long off = c.row_off(l, s, g, j0);
+        bulk_s2g(c.k + off, sk, (uint32_t)(rows * rb));
+        bulk_s2g(c.v + off, sk + (long long)ch * rb, (uint32_t)(rows * rb));
+      }
+    } else if (lane < rows) {
+      const long long off = c.row_off(l, s, g, j0 + lane);
+      if (off >= 0) {
+        bulk_s2g(c.k + off, sk + (long long)lane * rb, (uint32_t)rb);
+        bulk_s2g(c.v + off, sk + (long long)(ch + lane) * rb, (uint32_t)rb);
+      }
+    }
+    bulk_commit();
+    bulk_wait_read<1>();   // the stores of chunk cidx-1 no longer read their stage
+    __syncwarp();
+    if (cidx + kStages - 1 < nch) issue_loads(cidx + kStages - 1);   // refills that stage
   }
-  cp_async_wait<0>();
-  __syncthreads();
+  bulk_wait<0>();
+  return ok;
 }
 
 }  // namespace tri
