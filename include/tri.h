@@ -172,6 +172,39 @@ TRI_API tri_status tri_compress_step(const tri_cache *cache, const tri_stats *st
                              const tri_params *params, tri_compact_mode mode, int32_t *idx_out,
                              int32_t *new_len, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Size in bytes of the scratch array built into the library for
+ * tri_compress_step_static_scratch (32 MiB). */
+#define TRI_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* tri_compress_step for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a library convenience, not part of
+ * the method.  Some callers cannot call cudaMalloc: for example, a serving
+ * engine that gives nearly all device memory to its KV-cache pool at start-up
+ * and forbids later allocations, or code running in a plugin that has no
+ * access to the process's allocator.  Such a caller still owns the cache and
+ * the outputs but cannot supply the workspace that long units need.
+ *
+ * Same arguments and results as tri_compress_step, without ws/ws_bytes.  When
+ * the step needs scratch (tri_workspace_bytes > 0), it uses a file-scope
+ * device array of TRI_STATIC_SCRATCH_BYTES bytes that every GPU loading the
+ * library holds until the process exits.  A step that needs more than that
+ * returns TRI_ERR_WORKSPACE and launches nothing (no other limit differs).
+ * Nothing is allocated: no cudaMalloc, no cudaFree.
+ *
+ * Set-up: the first call on each device looks up that device's address of the
+ * array (with that device current), so make that first call before any stream
+ * capture begins.  A failed lookup returns TRI_ERR_CUDA.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents; the step writes each scratch entry before reading it, so
+ * nothing needs clearing.  Calls whose work overlaps on the GPU (two streams,
+ * or two host threads) race on the array and give wrong results: order them
+ * on one stream or with events. */
+TRI_API tri_status tri_compress_step_static_scratch(const tri_cache *cache, const tri_stats *stats,
+                                            const tri_params *params, tri_compact_mode mode,
+                                            int32_t *idx_out, int32_t *new_len,
+                                            cudaStream_t stream);
+
 /* Reads (and synchronises `stream` for) the device status word; *out (host)
  * receives TRI_OK or the first device-side error recorded since the last clear. */
 TRI_API tri_status tri_get_device_status(cudaStream_t stream, int32_t *out);

@@ -12,6 +12,7 @@ from .tri import (  # noqa: F401
     tri_clear_device_status,
     tri_compact_kv,
     tri_compress_step,
+    tri_compress_step_static_scratch,
     tri_get_device_status,
     tri_score,
     tri_select_topb,

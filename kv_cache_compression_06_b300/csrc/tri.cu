@@ -18,6 +18,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "tri_path.cuh"
 
@@ -660,6 +661,33 @@ static int bcap_of(const tri_cache *c, int budget) {
   return round32(budget < c->cap ? budget : c->cap);
 }
 
+// ---------------------------------------------------------------- built-in scratch
+// Scratch of tri_compress_step_static_scratch, for callers that cannot
+// allocate.  In host code `g_static_scratch` names a host-side stand-in, not
+// the device array: its device address is looked up per device below.
+static __device__ __align__(256) unsigned char g_static_scratch[TRI_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_static_mu;
+static void *g_static_addr[kMaxDevices];
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (with that device current) and cached.
+static tri_status static_scratch_addr(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TRI_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return TRI_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+      return TRI_ERR_CUDA;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return TRI_OK;
+}
+
 }  // namespace tri
 
 using namespace tri;
@@ -824,6 +852,23 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   sa.idx_out = idx_out;
   sa.new_len = new_len;
   return run_select_compact(sa, units, stream);
+}
+
+tri_status tri_compress_step_static_scratch(const tri_cache *cache, const tri_stats *stats,
+                                            const tri_params *params, tri_compact_mode mode,
+                                            int32_t *idx_out, int32_t *new_len,
+                                            cudaStream_t stream) {
+  tri_status e;
+  if ((e = check_cache(cache, true, true)) != TRI_OK) return e;
+  if (mode != TRI_COMPACT_ORDERED) return TRI_ERR_UNSUPPORTED;
+  size_t need = 0;
+  if ((e = tri_workspace_bytes(cache, stats, params, &need)) != TRI_OK) return e;
+  if (need == 0) return tri_compress_step(cache, stats, params, mode, idx_out, new_len, nullptr, 0, stream);
+  if (need > (size_t)TRI_STATIC_SCRATCH_BYTES) return TRI_ERR_WORKSPACE;
+  void *ws = nullptr;
+  if ((e = static_scratch_addr(&ws)) != TRI_OK) return e;
+  return tri_compress_step(cache, stats, params, mode, idx_out, new_len, ws,
+                           (size_t)TRI_STATIC_SCRATCH_BYTES, stream);
 }
 
 tri_status tri_get_device_status(cudaStream_t stream, int32_t *out) {

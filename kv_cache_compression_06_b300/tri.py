@@ -24,13 +24,15 @@ TRI_COMPACT_ORDERED = 0
 
 EXPORTED = ("tri_calibrate_stats", "tri_workspace_bytes", "tri_score", "tri_select_topb",
             "tri_compact_kv", "tri_compress_step", "tri_get_device_status",
-            "tri_clear_device_status", "tri_status_string", "tri_version")
+            "tri_clear_device_status", "tri_status_string", "tri_version",
+            "tri_compress_step_static_scratch")
 
 
 class TriError(RuntimeError):
-    def __init__(self, fn: str, status: int):
+    def __init__(self, fn: str, status: int, detail: str = ""):
         self.status = status
-        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+        msg = f"{fn}: {status_string(status)} (status {status})"
+        super().__init__(msg + (f": {detail}" if detail else ""))
 
 
 class tri_cache(ctypes.Structure):
@@ -70,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "tri_select_topb": [P, P, I, P, P, SZ, P],
             "tri_compact_kv": [P, P, I, I, P, P],
             "tri_compress_step": [P, P, P, I, P, P, P, SZ, P],
+            "tri_compress_step_static_scratch": [P, P, P, I, P, P, P],
             "tri_get_device_status": [P, ctypes.POINTER(ctypes.c_int32)],
             "tri_clear_device_status": [P],
             "tri_status_string": [I],
@@ -276,6 +279,31 @@ def tri_compress_step(cache: KVCache, stats: Stats, params: Params, idx_out: Opt
                                  _ptr(idx_out), _ptr(new_len), _ptr(ws), 0 if ws is None else ws.numel(),
                                  _stream(stream))
     _check("tri_compress_step", st)
+    return idx_out, new_len
+
+
+TRI_STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def tri_compress_step_static_scratch(cache: KVCache, stats: Stats, params: Params,
+                                     idx_out: Optional[torch.Tensor] = None,
+                                     new_len: Optional[torch.Tensor] = None, stream=None):
+    """tri_compress_step without a caller workspace, for callers that cannot
+    allocate device memory (e.g. an engine that reserved all of it for its
+    KV-cache pool).  Long units use the library's built-in scratch of
+    TRI_STATIC_SCRATCH_BYTES bytes, shared by every call on the device: calls
+    that overlap on the GPU race.  Make the first call on a device before any
+    stream capture (it looks up the scratch address)."""
+    c, s = cache.to_c(), stats.to_c()
+    p, _keep = params.to_c()
+    st = lib().tri_compress_step_static_scratch(ctypes.byref(c), ctypes.byref(s), ctypes.byref(p),
+                                                TRI_COMPACT_ORDERED, _ptr(idx_out), _ptr(new_len),
+                                                _stream(stream))
+    if st == TRI_ERR_WORKSPACE:
+        need = tri_workspace_bytes(cache, stats, params)
+        raise TriError("tri_compress_step_static_scratch", st,
+                       f"needs {need} bytes of scratch; the built-in scratch holds {TRI_STATIC_SCRATCH_BYTES}")
+    _check("tri_compress_step_static_scratch", st)
     return idx_out, new_len
 
 
