@@ -44,7 +44,8 @@ def _peaks():
 
 def _config(w, extra=None):
     c = {"workload": w.name, "layers": w.L, "kv_heads": w.Hkv, "q_heads": w.Hq, "head_dim": w.d,
-         "dtype_cache": w.dtype, "batch": w.S, "n_keys": w.n_keys, "budget": w.budget,
+         "dtype_cache": w.dtype, "batch": w.S, "n_keys": w.n_keys or list(w.n_range), "budget": w.budget,
+         "paged_block": w.block if w.paged else None,
          "offsets": f"2^0..2^{int(math.log2(max(w.offsets)))}", "theta": w.theta}
     if extra:
         c.update(extra)
@@ -153,14 +154,16 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ traffic record
-def _traffic_record(kernel_src_hash):
-    """Per-launch DRAM bytes of the fused kernel from the committed ncu summary,
-    if it was taken on the current kernel source (else None)."""
+def _traffic_record(kernel_src_hash, workload, layers):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source and this workload
+    (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f)
-        if rec.get("kernel_src_sha1") == kernel_src_hash and rec.get("workload") == WORKLOAD:
+        if (rec.get("kernel_src_sha1") == kernel_src_hash and rec.get("workload") == workload
+                and int(rec.get("layers", layers)) == layers):
             return float(rec["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -177,6 +180,18 @@ def kernel_src_hash():
 
 
 # ------------------------------------------------------------------ GPU leg
+def _moved_rows(idx, seq_len, B):
+    """Rows each compressed unit actually moves: B minus the untouched prefix
+    (idx_j == j), summed over units with N > B."""
+    import torch
+    ii = idx.view(-1, B).long()
+    ar = torch.arange(B, device=ii.device)
+    e0 = torch.where((ii != ar).any(dim=1), (ii != ar).int().argmax(dim=1), torch.full_like(ii[:, 0], B))
+    L, S, Hkv = idx.shape[0], idx.shape[1], idx.shape[2]
+    n = seq_len.long().view(1, S, 1).expand(L, S, Hkv).reshape(-1)
+    return int(torch.where(n > B, B - e0, torch.zeros_like(e0)).sum())
+
+
 def run_b300(args, w):
     import torch
     import torch.distributed as dist
@@ -189,30 +204,39 @@ def run_b300(args, w):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     # CPU oracle baseline first (rank 0, N=1), before any GPU work.
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and w.name == WORKLOAD:
         keys, el, units, cores = oracle_sample(w, args.cpu_seconds)
         cpu = {"value": keys / el, "unit": "keys/s", "cores": cores, "kind": "oracle",
-               "sample": f"{units} random units (seq, KV head) of layer 0, N=2176 keys each, "
+               "sample": f"{units} random units (seq, KV head) of layer 0, {keys} keys in all, "
                          f"{el:.1f} s; per-offset route, fp64 numpy, 1 thread"}
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     data = generate(w, device=dev)
-    cache = tk.KVCache(data["k"], data["v"], data["seq_len"], Hkv=w.Hkv)
-    stats = tk.tri_calibrate_stats(data["q_pre"])
+    cache = tk.KVCache(data["k"], data["v"], data["seq_len"], Hkv=w.Hkv,
+                       block_table=data.get("block_table"), block=w.block)
+    stats = tk.tri_calibrate_stats(data["q_pre"], pairing=w.pairing)
     del data["q_pre"]
-    params = tk.Params(w.theta, data["t"], w.offsets, w.budget)
+    params = tk.Params(w.theta, data["t"], w.offsets, w.budget, pairing=w.pairing)
     ws = tk.workspace(cache, stats, params)
     launches = 1 if ws is None else 2
     k0, v0 = cache.k.clone(), cache.v.clone()
-    idx = torch.empty((w.L, w.S, w.Hkv, w.budget), dtype=torch.int32, device=dev)
+    L = cache.L
+    idx = torch.empty((L, w.S, w.Hkv, w.budget), dtype=torch.int32, device=dev)
     new_len = torch.empty(w.S, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
+
+    # A cache smaller than L2 (126 MB) would stay resident across steps: write a
+    # 256 MB buffer after each restore so every step starts from a cold L2.
+    cache_bytes = 2 * k0.numel() * k0.element_size()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if cache_bytes < (512 << 20) else None
 
     def restore():
         cache.k.copy_(k0)
         cache.v.copy_(v0)
+        if flush is not None:
+            flush.fill_(1)
 
     def step():
         tk.tri_compress_step(cache, stats, params, idx_out=idx, new_len=new_len, ws=ws, stream=stream)
@@ -223,16 +247,17 @@ def run_b300(args, w):
     torch.cuda.synchronize()
     assert tk.tri_get_device_status() == 0
 
-    # algorithmic bytes: K read for scoring + K/V moved (read + write) by compaction
+    # algorithmic bytes: K read for scoring + K/V moved (read + write) by
+    # compaction, over the units the step compresses (N > B)
     B, rb = w.budget, w.d * w.esize
-    ii = idx.view(-1, B).long()
-    ar = torch.arange(B, device=dev)
-    e0 = torch.where((ii != ar).any(dim=1), (ii != ar).int().argmax(dim=1), torch.full_like(ii[:, 0], B))
-    M = int((B - e0).clamp_min(0).sum())
-    units = w.L * w.S * w.Hkv
-    n_keys = units * w.n_keys
-    alg_bytes = n_keys * rb + 4 * M * rb
-    alg_bytes_full_move = n_keys * rb + 4 * units * B * rb
+    lens = [int(x) for x in data["seq_len"].tolist()]
+    M = _moved_rows(idx, data["seq_len"], B)
+    units = L * w.S * w.Hkv
+    n_keys = L * w.Hkv * sum(lens)
+    scored = L * w.Hkv * sum(n for n in lens if n > B)
+    units_c = L * w.Hkv * sum(1 for n in lens if n > B)
+    alg_bytes = scored * rb + 4 * M * rb
+    alg_bytes_full_move = scored * rb + 4 * units_c * B * rb
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
@@ -258,29 +283,33 @@ def run_b300(args, w):
     assert tk.tri_get_device_status() == 0
 
     # end to end through the public API from pinned host buffers
-    hk = torch.empty_like(k0, device="cpu").pin_memory()
-    hv = torch.empty_like(v0, device="cpu").pin_memory()
-    hk.copy_(k0)
-    hv.copy_(v0)
-    ok_ = torch.empty_like(hk).pin_memory()
-    ov = torch.empty_like(hv).pin_memory()
-    oi = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
-    on = torch.empty(new_len.shape, dtype=torch.int32).pin_memory()
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        cache.k.copy_(hk, non_blocking=True)
-        cache.v.copy_(hv, non_blocking=True)
-        step()
-        ok_.copy_(cache.k, non_blocking=True)
-        ov.copy_(cache.v, non_blocking=True)
-        oi.copy_(idx, non_blocking=True)
-        on.copy_(new_len, non_blocking=True)
-    torch.cuda.synchronize()
-    t_e2e = (time.perf_counter() - t0) / e2e_steps
-    h2d = hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
-    d2h = h2d + oi.numel() * 4 + on.numel() * 4
+    e2e = None
+    if args.e2e_steps > 0:
+        hk = torch.empty_like(k0, device="cpu").pin_memory()
+        hv = torch.empty_like(v0, device="cpu").pin_memory()
+        hk.copy_(k0)
+        hv.copy_(v0)
+        ok_ = torch.empty_like(hk).pin_memory()
+        ov = torch.empty_like(hv).pin_memory()
+        oi = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
+        on = torch.empty(new_len.shape, dtype=torch.int32).pin_memory()
+        e2e_steps = min(args.steps, args.e2e_steps)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            cache.k.copy_(hk, non_blocking=True)
+            cache.v.copy_(hv, non_blocking=True)
+            step()
+            ok_.copy_(cache.k, non_blocking=True)
+            ov.copy_(cache.v, non_blocking=True)
+            oi.copy_(idx, non_blocking=True)
+            on.copy_(new_len, non_blocking=True)
+        torch.cuda.synchronize()
+        t_e2e = (time.perf_counter() - t0) / e2e_steps
+        h2d = hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
+        d2h = h2d + oi.numel() * 4 + on.numel() * 4
+        e2e = {"value": world * n_keys / t_e2e, "unit": "keys/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
     if rank != 0:
         if world > 1:
@@ -288,26 +317,29 @@ def run_b300(args, w):
         return
     peak, peak_kind = _peaks()
     achieved = alg_bytes / t_step / 1e9
+    kname = f"fused_kernel<{w.d},{w.G},{w.dtype}>" if launches == 1 else "score_tiles_kernel+select_compact_kernel"
     line = {
         "metric": METRIC, "value": world * n_keys / t_step, "unit": "keys/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": _config(w, {"l2": f"cache restored from a pristine {2 * k0.numel() * 2 / 1e9:.1f} GB copy "
-                                    "before every step (flushes L2; untimed)", "parallelism": f"replicas x{world}"}),
+        "config": _config(w, {"layers": L,
+                              "l2": f"cache restored from a pristine {cache_bytes / 1e9:.3f} GB copy before every "
+                                    "step" + (" plus a 256 MB L2 flush" if flush is not None else " (flushes L2)")
+                                    + "; untimed",
+                              "parallelism": f"replicas x{world}"}),
         "compress_step_us": t_step * 1e6,
         "hbm_gbs": achieved,
         "hbm_frac_of_8tbs": achieved / 8000.0,
-        "moved_rows": M, "moved_rows_if_all_B": units * B,
+        "moved_rows": M, "moved_rows_if_all_B": units_c * B, "units": units, "units_compressed": units_c,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": _traffic_record(kernel_src_hash()),
+                     "traffic": _traffic_record(kernel_src_hash(), w.name, L),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "algorithmic_bytes_if_all_B_moved": alg_bytes_full_move,
-                     "kernel": "fused_kernel<128,4,bf16>" if launches == 1 else "score_tiles+select_compact"},
+                     "kernel": kname},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * n_keys / t_e2e, "unit": "keys/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "e2e": e2e,
         "clocks": clk.summary(),
         "gpu_launches": launches * args.steps,
         "step_ms_min": min(ms), "step_ms_median": float(np.median(ms)),
@@ -324,15 +356,23 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=3,
+                    help="end-to-end steps from pinned host buffers (0: skip; the host needs 4x the cache size)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload name (default: the 36-layer Qwen3-8B-shaped batch-16 step)")
     ap.add_argument("--layers", type=int, default=None,
-                    help="use only the first N layers (small case for ncu captures; default: all 36)")
+                    help="use only the first N layers (small case for ncu captures, or a layer group "
+                         "of a workload whose full cache exceeds HBM)")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="use only N sequences (small case for ncu captures)")
     args = ap.parse_args()
     from synth import WORKLOADS
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     if args.layers:
         w = w.with_(L=args.layers)
+    if args.seqs:
+        w = w.with_(S=args.seqs)
     if args.impl == "reference":
         run_reference(args, w)
     else:

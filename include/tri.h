@@ -37,7 +37,8 @@
  * Conventions for every entry point.
  *   - All pointers are DEVICE pointers unless marked (host).  The caller owns
  *     every buffer; the library allocates nothing.  Scratch comes from the
- *     caller's workspace, sized by tri_workspace_bytes().
+ *     caller's workspace, sized by tri_workspace_bytes() and 16-byte aligned
+ *     (cudaMalloc alignment satisfies this).
  *   - Work is enqueued asynchronously on `stream`; nothing synchronises.
  *   - Arguments are validated on the host first: a bad argument returns
  *     TRI_ERR_INVALID, a valid but unsupported shape TRI_ERR_UNSUPPORTED, a too
@@ -72,7 +73,7 @@ typedef enum {
   TRI_ERR_INVALID = 1,      /* bad argument (host) or bad device-side data      */
   TRI_ERR_CUDA = 2,         /* a CUDA runtime call failed                       */
   TRI_ERR_UNSUPPORTED = 3,  /* valid but not implemented (d, G, sizes)          */
-  TRI_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required       */
+  TRI_ERR_WORKSPACE = 4,    /* workspace missing, too small or misaligned       */
   TRI_ERR_TIMEOUT = 5,      /* a bounded device wait gave up                    */
   TRI_ERR_BOUNDS = 6        /* device-side index check failed (block id, N>cap) */
 } tri_status;

@@ -7,11 +7,12 @@
 // Kernels
 //   calib_kernel         a0: per (layer, query head): center, mean |q_f|, R.
 //   fused_kernel         a1..a5 for units whose scores fit one CTA's shared
-//                        memory: weights -> TMA-streamed scoring -> z/max ->
-//                        radix top-B -> in-place cp.async compaction.  Also the
-//                        score-only variant behind tri_score.
-//   score_tiles_kernel   a1+a2 for long units, 2048 keys per CTA: raw scores and
-//                        per-tile (mean, M2) to the workspace.
+//                        memory: weights -> TMA-streamed scoring (producer warp +
+//                        8 consumer warps) -> z/max -> radix top-B -> in-place
+//                        bulk-copy compaction.  Also the score-only variant
+//                        behind tri_score.
+//   score_tiles_kernel   a1+a2 for long units, 2048 keys per CTA (same pipeline):
+//                        raw scores and per-tile (mean, M2) to the workspace.
 //   zmax_kernel          a3 for long units (tri_score): Chan-merged moments -> agg.
 //   select_compact_kernel a3..a5 for long units (from raw scores), tri_select_topb
 //                        (from agg) and tri_compact_kv (from idx).
@@ -83,6 +84,8 @@ __global__ void __launch_bounds__(256) calib_kernel(const void *q, int bf16, lon
 }
 
 // ---------------------------------------------------------------- fused short-unit kernel
+// One CTA of kFusedThreads per unit: score (every warp; warp 0 refills the
+// ring), z/max, select, compact.  Two CTAs per SM for G <= 4.
 struct FusedArgs {
   CacheView c;
   const float *center, *R, *mag;
@@ -104,7 +107,7 @@ struct FusedLayout {
     int o = kRingBytes;
     bars = o;   o += 128;                 // kStages score barriers + kStages compaction barriers
     wts = o;    o += align_up(G * 3 * F * 4, 128);
-    red = o;    o += 256;
+    red = o;    o += 512;
     hist = o;   o += 1024;
     sm = o;     o += 256;
     scores = o; o += align_up(G * sstride * 4, 128);
@@ -119,7 +122,7 @@ struct FusedLayout {
 };
 
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1)) fused_kernel(const FusedArgs a) {
+__global__ void __launch_bounds__(kFusedThreads, (G <= 4 ? 2 : 1)) fused_kernel(const FusedArgs a) {
   constexpr int F = D / 2;
   extern __shared__ __align__(1024) char smem[];
   const FusedLayout lay(G, F, a.capp);
@@ -191,24 +194,38 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1)) fused_kernel(const
   if (a.mode == 1) return;
   __syncthreads();
   int ntie;
-  const uint32_t T = radix_select(keys, N, B, hist, sm, &ntie);
-  const int e0 = build_kept(keys, N, B, T, ntie, idxs, sm);
+  const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
+  const int e0 = build_kept_chunked(keys, N, B, T, ntie, idxs, sm);
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
   // The ring was last read by generic loads (scoring); TMA writes it next.
   fence_proxy_async_smem();
   __syncthreads();
-  if ((tid >> 5) == 0) compact_unit_tma(c, l, s, g, idxs, e0, B, N, ring, bars + kStages);
+  if ((tid >> 5) == 0) compact_unit_runs(c, l, s, g, idxs, e0, B, N, ring, bars + kStages);
+}
+
+// Pipe over the barrier block of a layout: full[4] | empty[4] | compaction[4] | fail, issued.
+__device__ __forceinline__ Pipe make_pipe(char *smem, int bars) {
+  uint64_t *b = reinterpret_cast<uint64_t *>(smem + bars);
+  Pipe p;
+  p.ring = smem;
+  p.full = b;
+  p.empty = b + kStages;
+  p.fail = reinterpret_cast<volatile int *>(b + 3 * kStages);
+  p.issued = p.fail + 1;
+  return p;
 }
 
 // ---------------------------------------------------------------- long units: tiles
 struct TileArgs {
+  TmaMaps maps;      // as in FusedArgs (k4 only is used)
   CacheView c;
   const float *center, *R, *mag;
   int Hq;
   const int *t;
   int budget, skip_small, inter, ntiles;
-  float *raw;      // [(u*G + h)*cap + i]
+  long long raw_stride;   // floats between the raw rows of two heads (cap, or capp in the workspace)
+  float *raw;      // [(u*G + h)*raw_stride + i]
   float2 *part;    // [(u*ntiles + tile)*G + h] = (mean, M2) of the tile
   StepConst sc;
 };
@@ -221,7 +238,7 @@ struct TileLayout {
     int o = kRingBytes;
     bars = o;   o += 128;
     wts = o;    o += align_up(G * 3 * F * 4, 128);
-    red = o;    o += 256;
+    red = o;    o += 512;
     scores = o; o += G * kTileStride * 4;
     total = o;
   }
@@ -256,12 +273,12 @@ __device__ __forceinline__ void head_mean_m2(const float *scores, int stride, in
 }
 
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1)) score_tiles_kernel(const TileArgs a) {
+__global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
+    score_tiles_kernel(const __grid_constant__ TileArgs a) {
   constexpr int F = D / 2;
   extern __shared__ __align__(1024) char smem[];
   const TileLayout lay(G, F);
-  char *ring = smem;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  const Pipe pipe = make_pipe(smem, lay.bars);
   float *wts = reinterpret_cast<float *>(smem + lay.wts);
   float *red = reinterpret_cast<float *>(smem + lay.red);
   float *scores = reinterpret_cast<float *>(smem + lay.scores);
@@ -278,24 +295,21 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1)) score_tiles_kernel
   const int i0 = tile * kTileKeys;
   if (i0 >= N) return;
   const int n = min(kTileKeys, N - i0);
-  if (!c.blocks_ok(s, N)) {
+  if (!c.blocks_ok(s, n, i0)) {
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
-  if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 32);
-    fence_mbar_init();
-  }
+  if (tid == 0) pipe_init(pipe);
   build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc);
   __syncthreads();
   LaneWeights<G> lw;
   load_lane_weights<G, F>(lw, wts, (tid & 31) % RowGeom<D, BF16>::LPR);
-  if (!score_unit_rows<D, G, BF16>(c, l, s, g, i0, n, ring, bars, scores, kTileStride, lw,
-                                   a.inter != 0))
+  if (!stream_and_score<D, G, BF16>(c, &a.maps.k4, l, s, g, i0, n, pipe, scores, kTileStride, lw,
+                                    a.inter != 0))
     return;
   for (int i = tid; i < n; i += nt) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * c.cap + i0 + i] = scores[h * kTileStride + i];
+    for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * a.raw_stride + i0 + i] = scores[h * kTileStride + i];
   }
   float mu[G], m2[G];
   head_mean_m2<G>(scores, kTileStride, n, red, mu, m2);
@@ -306,37 +320,61 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1)) score_tiles_kernel
   }
 }
 
-// Chan's parallel combination of per-tile (count, mean, M2), in fp64; thread h < G
-// writes mean and 1/std (0 if std = 0) of head h to mom[h], mom[8 + h].
-__device__ __forceinline__ void merge_tile_moments(const float2 *part, long long u, int ntiles,
-                                                   int G, int N, float *mom) {
-  const int h = threadIdx.x;
-  if (h < G) {
-    double n = 0, mean = 0, M2 = 0;
-    const int nt = (N + kTileKeys - 1) / kTileKeys;
-    for (int t = 0; t < nt; ++t) {
-      const double nb = (double)min(kTileKeys, N - t * kTileKeys);
-      const float2 p = part[(u * ntiles + t) * G + h];
-      if (n == 0) {
-        n = nb;
-        mean = p.x;
-        M2 = p.y;
-      } else {
-        const double tot = n + nb, dl = (double)p.x - mean;
-        mean += dl * nb / tot;
-        M2 += (double)p.y + dl * dl * n * nb / tot;
-        n = tot;
-      }
+// Chan's combination of (count, mean, M2) summaries: (n, mean, M2) absorbs (nb, mb, Mb).
+__device__ __forceinline__ void chan_merge(float &n, float &mean, float &M2, float nb, float mb, float Mb) {
+  if (nb <= 0.f) return;
+  if (n <= 0.f) {
+    n = nb;
+    mean = mb;
+    M2 = Mb;
+    return;
+  }
+  const float tot = n + nb, dl = mb - mean;
+  mean = fmaf(dl, nb / tot, mean);
+  M2 = M2 + Mb + dl * dl * (n * nb / tot);
+  n = tot;
+}
+
+// Merges the per-tile (mean, M2) of a unit's N keys; warp h < G handles head h
+// (lanes take tiles lane, lane + 32, ..., then a butterfly of Chan merges) and
+// writes mean and 1/std (0 if std = 0) to mom[h], mom[8 + h].  Needs blockDim
+// >= 32 * G; the caller synchronises before reading mom.
+__device__ __forceinline__ void merge_tile_moments(const float2 *part, long long u, int ntiles, int G,
+                                                   int N, float *mom) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= G) return;
+  const int h = warp;
+  const int used = (N + kTileKeys - 1) / kTileKeys;
+  float n = 0.f, mean = 0.f, M2 = 0.f;
+  for (int t = lane; t < used; t += 32) {
+    const float2 p = part[(u * ntiles + t) * G + h];
+    chan_merge(n, mean, M2, (float)min(kTileKeys, N - t * kTileKeys), p.x, p.y);
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float n2 = __shfl_xor_sync(0xffffffffu, n, o);
+    const float m2 = __shfl_xor_sync(0xffffffffu, mean, o);
+    const float q2 = __shfl_xor_sync(0xffffffffu, M2, o);
+    if (lane & o)
+      chan_merge(n, mean, M2, n2, m2, q2);   // both partners merge in the same order
+    else {
+      float a = n2, b = m2, cq = q2;
+      chan_merge(a, b, cq, n, mean, M2);
+      n = a;
+      mean = b;
+      M2 = cq;
     }
-    const double sd = sqrt(M2 / n);
-    mom[h] = (float)mean;
-    mom[8 + h] = sd > 0 ? (float)(1.0 / sd) : 0.0f;
+  }
+  if (lane == 0) {
+    const float sd = sqrtf(M2 / n);
+    mom[h] = mean;
+    mom[8 + h] = sd > 0.f ? 1.0f / sd : 0.0f;
   }
 }
 
 struct ZArgs {
   int S, Hkv, G, ntiles;
-  long long cap;
+  long long cap, raw_stride;
   const int *seq_len;
   const float *raw;
   const float2 *part;
@@ -357,7 +395,7 @@ __global__ void __launch_bounds__(256) zmax_kernel(const ZArgs a) {
   for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
     float z = -INFINITY;
     for (int h = 0; h < a.G; ++h) {
-      const float zh = (a.raw[((long long)u * a.G + h) * a.cap + i] - mom[h]) * mom[8 + h];
+      const float zh = (a.raw[((long long)u * a.G + h) * a.raw_stride + i] - mom[h]) * mom[8 + h];
       z = h == 0 ? zh : fmaxf(z, zh);
     }
     a.agg[(long long)u * a.cap + i] = z;
@@ -366,32 +404,97 @@ __global__ void __launch_bounds__(256) zmax_kernel(const ZArgs a) {
 
 // ---------------------------------------------------------------- select / compact
 struct SCArgs {
+  TmaMaps maps;
   CacheView c;
   int G, budget, mode, ntiles, capp, bcap;   // mode 0: from raw (+compact), 1: from agg, 2: compact idx
-  const float *raw;
+  const float *raw;     // mode 0: workspace [(u*G + h)*capp + i], rows 16-byte aligned
   const float2 *part;
   const float *agg;
   const int *idx_in;
   int *idx_out, *new_len;
 };
 
+// The keys region follows the ring directly: once the kept list is built the
+// keys are dead and the compaction ring extends over them (nstages stages).
+// A compaction-only launch (capp = 0) reserves `extra` bytes there instead.
 struct SCLayout {
-  int bars, hist, sm, mom, keys, idx, total;
-  __host__ __device__ SCLayout(int capp, int bcap) {
+  int keys, bars, hist, sm, mom, idx, nstages, total;
+  __host__ __device__ SCLayout(int capp, int bcap, int extra) {
     int o = kRingBytes;
-    bars = o; o += 128;
+    keys = o;
+    const int kb = align_up(capp * 4 > extra ? capp * 4 : extra, 128);
+    o += kb;
+    nstages = min(kMaxCompactStages, (kRingBytes + kb) / kStageBytes);
+    bars = o; o += kMaxCompactStages * 8;
     hist = o; o += 1024;
-    sm = o;   o += 256;
+    sm = o;   o += kSelInts * 4;
     mom = o;  o += 128;
-    keys = o; o += align_up(capp * 4, 128);
     idx = o;  o += align_up(bcap * 4, 128);
     total = o;
   }
 };
 
-__global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const SCArgs a) {
+constexpr int kCompactOnlyExtra = 2 * kRingBytes;   // compaction-only ring: 12 stages
+
+// a3 for one long unit from its raw scores: the G rows raw[h][0..N) (stride
+// capp floats, 16-byte aligned) are read with 16-byte loads, U*G of them in
+// flight per thread; every thread turns its keys into z = max_h (s_h - mean_h) /
+// std_h, writes the order-preserving keys (4 per store) and adds them to the
+// top-byte histogram.  Key slots in [N, round4(N)) receive don't-care values.
+template <int G>
+__device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *mom, uint32_t *keys,
+                              uint32_t *hist) {
+  constexpr int U = G >= 8 ? 1 : 8 / G;
+  const int tid = threadIdx.x, lane = tid & 31, nt = blockDim.x;
+  float mu[G], iv[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    mu[h] = mom[h];
+    iv[h] = mom[8 + h];
+  }
+  const int n4 = (N + 3) / 4;
+  for (int base = tid & ~31; base < n4; base += nt * U) {
+    float4 v[U][G];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int q = base + k * nt + lane;
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        v[k][h] = q < n4 ? __ldg(reinterpret_cast<const float4 *>(raw_u + (long long)h * capp) + q)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int q = base + k * nt + lane;
+      float z[4];
+      z[0] = (v[k][0].x - mu[0]) * iv[0];
+      z[1] = (v[k][0].y - mu[0]) * iv[0];
+      z[2] = (v[k][0].z - mu[0]) * iv[0];
+      z[3] = (v[k][0].w - mu[0]) * iv[0];
+#pragma unroll
+      for (int h = 1; h < G; ++h) {
+        z[0] = fmaxf(z[0], (v[k][h].x - mu[h]) * iv[h]);
+        z[1] = fmaxf(z[1], (v[k][h].y - mu[h]) * iv[h]);
+        z[2] = fmaxf(z[2], (v[k][h].z - mu[h]) * iv[h]);
+        z[3] = fmaxf(z[3], (v[k][h].w - mu[h]) * iv[h]);
+      }
+      uint4 kk;
+      kk.x = score_key(z[0]);
+      kk.y = score_key(z[1]);
+      kk.z = score_key(z[2]);
+      kk.w = score_key(z[3]);
+      if (q < n4) reinterpret_cast<uint4 *>(keys)[q] = kk;
+      hist_add_top(hist, kk.x, 4 * q + 0 < N);
+      hist_add_top(hist, kk.y, 4 * q + 1 < N);
+      hist_add_top(hist, kk.z, 4 * q + 2 < N);
+      hist_add_top(hist, kk.w, 4 * q + 3 < N);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __grid_constant__ SCArgs a) {
   extern __shared__ __align__(1024) char smem[];
-  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap);
+  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap, a.mode == 2 ? kCompactOnlyExtra : 0);
   char *ring = smem;
   uint64_t *cbars = reinterpret_cast<uint64_t *>(smem + lay.bars);
   uint32_t *hist = reinterpret_cast<uint32_t *>(smem + lay.hist);
@@ -400,7 +503,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const SC
   uint32_t *keys = reinterpret_cast<uint32_t *>(smem + lay.keys);
   int *idxs = reinterpret_cast<int *>(smem + lay.idx);
   const CacheView &c = a.c;
-  const int tid = threadIdx.x, nt = blockDim.x;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
   const int u = blockIdx.x;
   const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
   const int N = c.seq_len[s];
@@ -420,7 +523,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const SC
     return;
   }
   if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&cbars[st], 1);
+    for (int st = 0; st < lay.nstages; ++st) mbar_init(&cbars[st], 1);
     fence_mbar_init();
   }
   if (a.mode == 2) {
@@ -431,42 +534,52 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const SC
       idxs[j] = v;
       bad |= (v < 0) | (v >= N) | (j > 0 && v <= src[j - 1]);
     }
-    if (tid == 0) sm[36] = B;
+    if (tid == 0) sm[56] = B;
     if (__syncthreads_or(bad)) {
       if (tid == 0) set_status(TRI_ERR_INVALID);
       return;
     }
     for (int j = tid; j < B; j += nt)
-      if (idxs[j] != j) atomicMin(&sm[36], j);
+      if (idxs[j] != j) atomicMin(&sm[56], j);
     __syncthreads();
-    const int e0 = sm[36];
+    const int e0 = sm[56];
     __syncthreads();
-    if ((tid >> 5) == 0) compact_unit_tma(c, l, s, g, idxs, e0, B, N, ring, cbars);
+    if ((tid >> 5) == 0) compact_unit_tma(c, &a.maps, l, s, g, idxs, e0, B, N, ring, lay.nstages, cbars);
     return;
   }
+  for (int b = tid; b < 256; b += nt) hist[b] = 0;
   if (a.mode == 0) {
     merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom);
     __syncthreads();
-    for (int i = tid; i < N; i += nt) {
-      float z = 0.f;
-      for (int h = 0; h < a.G; ++h) {
-        const float zh = (a.raw[((long long)u * a.G + h) * c.cap + i] - mom[h]) * mom[8 + h];
-        z = h == 0 ? zh : fmaxf(z, zh);
-      }
-      keys[i] = score_key(z);
+    const float *raw_u = a.raw + (long long)u * a.G * a.capp;
+    switch (a.G) {
+      case 1: zmax_from_raw<1>(raw_u, a.capp, N, mom, keys, hist); break;
+      case 2: zmax_from_raw<2>(raw_u, a.capp, N, mom, keys, hist); break;
+      case 4: zmax_from_raw<4>(raw_u, a.capp, N, mom, keys, hist); break;
+      default: zmax_from_raw<8>(raw_u, a.capp, N, mom, keys, hist); break;
     }
+    __syncthreads();
   } else {
-    for (int i = tid; i < N; i += nt) keys[i] = score_key(a.agg[(long long)u * c.cap + i]);
+    __syncthreads();
+    for (int base = tid & ~31; base < N; base += nt) {
+      const int i = base + lane;
+      const uint32_t key = i < N ? score_key(a.agg[(long long)u * c.cap + i]) : 0u;
+      if (i < N) keys[i] = key;
+      hist_add_top(hist, key, i < N);
+    }
+    __syncthreads();
   }
-  __syncthreads();
   int ntie;
-  const uint32_t T = radix_select(keys, N, B, hist, sm, &ntie);
+  const uint32_t T = radix_select(keys, N, B, hist, sm, &ntie, true);
   const int e0 = build_kept(keys, N, B, T, ntie, idxs, sm);
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
   if (a.mode == 0) {
+    // The ring extends over the keys, last accessed by generic loads and
+    // stores; TMA writes them next.
+    fence_proxy_async_smem();
     __syncthreads();
-    if ((tid >> 5) == 0) compact_unit_tma(c, l, s, g, idxs, e0, B, N, ring, cbars);
+    if ((tid >> 5) == 0) compact_unit_tma(c, &a.maps, l, s, g, idxs, e0, B, N, ring, lay.nstages, cbars);
   }
 }
 
@@ -524,7 +637,81 @@ static CacheView make_view(const tri_cache *c) {
   v.max_blocks = c->block_table ? c->max_blocks : 0;
   v.block = c->block_table ? c->block : 1;
   v.nblocks = c->block_table ? c->nblocks : 0;
+  v.tm_ok = 0;
+  v.g4_ok = 0;
   return v;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no link against libcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Tensor map over a paged pool [L][nblocks][block][Hkv][d] whose box is one
+// block of one head ({d, 1, block, 1}), for the per-stage K loads and the
+// per-block compaction stores.  Used only when a score stage holds a whole
+// number of blocks (at most 32 of them); returns false otherwise or if encoding
+// fails (per-row copies are used instead).
+static bool make_block_map(const tri_cache *c, void *base, CUtensorMap *map) {
+  if (c->block_table == nullptr) return false;
+  const int es = c->dtype == TRI_BF16 ? 2 : 4;
+  const int rb = c->d * es;
+  const int tr = kStageBytes / rb;
+  if (c->block > 256 || tr % c->block != 0 || tr / c->block > 32) return false;
+  if ((int64_t)c->L * c->nblocks >= (1ll << 31)) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)c->d, (cuuint64_t)c->Hkv, (cuuint64_t)c->block,
+                              (cuuint64_t)c->L * (cuuint64_t)c->nblocks};
+  const cuuint64_t strides[3] = {(cuuint64_t)rb, (cuuint64_t)c->Hkv * rb, (cuuint64_t)c->block * c->Hkv * rb};
+  const cuuint32_t box[4] = {(cuuint32_t)c->d, 1u, (cuuint32_t)c->block, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = enc(map, c->dtype == TRI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                         4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Tensor map viewing the K or V storage as rows [rows][d] (dense: L*S*Hkv*cap
+// rows; paged: L*nblocks*block*Hkv pool rows) with a box of one row, for the
+// tile::gather4 loads of the compaction.  Row coordinates are int32, so the
+// view must have fewer than 2^31 rows; returns false otherwise or on failure.
+static bool make_row_map(const tri_cache *c, void *base, CUtensorMap *map) {
+  const int es = c->dtype == TRI_BF16 ? 2 : 4;
+  const int rb = c->d * es;
+  const int64_t rows = c->block_table == nullptr ? (int64_t)c->L * c->S * c->Hkv * c->cap
+                                                 : (int64_t)c->L * c->nblocks * c->block * c->Hkv;
+  if (rows < 1 || rows >= (1ll << 31)) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)c->d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)rb};
+  const cuuint32_t box[2] = {(cuuint32_t)c->d, 1u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, c->dtype == TRI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                         2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Builds the tensor maps of a call and sets the view's flags.  K and V maps
+// are made together; a V map is needed only when V is given (compaction).
+static void make_maps(const tri_cache *c, CacheView *v, TmaMaps *m) {
+  std::memset(m, 0, sizeof(*m));
+  v->tm_ok = make_block_map(c, c->k, &m->k4) && (c->v == nullptr || make_block_map(c, c->v, &m->v4));
+  v->g4_ok = c->k != nullptr && c->v != nullptr && make_row_map(c, c->k, &m->k2) && make_row_map(c, c->v, &m->v2);
 }
 
 static StepConst make_const(const tri_params *p, int d) {
@@ -556,7 +743,8 @@ struct SplitWs {
 };
 static SplitWs split_ws(const tri_cache *c, int G) {
   SplitWs w;
-  const size_t raw = (size_t)units_of(c) * G * (size_t)c->cap * sizeof(float);
+  // raw rows padded to round32(cap) floats: 16-byte aligned for bulk copies
+  const size_t raw = (size_t)units_of(c) * G * (size_t)round32(c->cap) * sizeof(float);
   const size_t part = (size_t)units_of(c) * ntiles_of(c) * G * sizeof(float2);
   w.raw_off = 0;
   w.part_off = (raw + 255) / 256 * 256;
@@ -580,7 +768,7 @@ static tri_status run_fused(const FusedArgs &a, int64_t units, cudaStream_t st) 
   const FusedLayout lay(G, D / 2, a.capp);
   auto k = fused_kernel<D, G, BF16>;
   if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
-  k<<<(unsigned)units, kThreads, lay.total, st>>>(a);
+  k<<<(unsigned)units, kFusedThreads, lay.total, st>>>(a);
   return launch_result();
 }
 
@@ -618,7 +806,7 @@ static tri_status run_tiles(const TileArgs &a, int64_t units, cudaStream_t st) {
   }()
 
 static tri_status run_select_compact(const SCArgs &a, int64_t units, cudaStream_t st) {
-  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap);
+  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap, a.mode == 2 ? kCompactOnlyExtra : 0);
   if (lay.total > kMaxSmem) return TRI_ERR_UNSUPPORTED;
   if (set_smem(select_compact_kernel, lay.total) != TRI_OK) return TRI_ERR_CUDA;
   select_compact_kernel<<<(unsigned)units, kSelThreads, lay.total, st>>>(a);
@@ -654,6 +842,7 @@ static TileArgs tile_args(const tri_cache *c, const tri_stats *stt, const tri_pa
   a.inter = p->pairing == TRI_PAIR_INTERLEAVED;
   a.ntiles = ntiles_of(c);
   a.sc = make_const(p, c->d);
+  make_maps(c, &a.c, &a.maps);
   return a;
 }
 
@@ -753,10 +942,11 @@ tri_status tri_score(const tri_cache *cache, const tri_stats *stats, const tri_p
     return TRI_DISPATCH(run_fused, cache->d, G, bf16, a, units, stream);
   }
   const SplitWs w = split_ws(cache, G);
-  if (ws == nullptr || ws_bytes < w.total) return TRI_ERR_WORKSPACE;
+  if (ws == nullptr || ws_bytes < w.total || !aligned16(ws)) return TRI_ERR_WORKSPACE;
   TileArgs ta = tile_args(cache, stats, params);
   ta.skip_small = 0;
   ta.raw = raw != nullptr ? raw : reinterpret_cast<float *>(static_cast<char *>(ws) + w.raw_off);
+  ta.raw_stride = raw != nullptr ? cache->cap : round32(cache->cap);
   ta.part = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.part_off);
   if ((e = TRI_DISPATCH(run_tiles, cache->d, G, bf16, ta, units, stream)) != TRI_OK) return e;
   ZArgs z;
@@ -765,6 +955,7 @@ tri_status tri_score(const tri_cache *cache, const tri_stats *stats, const tri_p
   z.G = G;
   z.ntiles = ta.ntiles;
   z.cap = cache->cap;
+  z.raw_stride = ta.raw_stride;
   z.seq_len = cache->seq_len;
   z.raw = ta.raw;
   z.part = ta.part;
@@ -802,6 +993,7 @@ tri_status tri_compact_kv(const tri_cache *cache, const int32_t *idx, int budget
   SCArgs a;
   std::memset(&a, 0, sizeof(a));
   a.c = make_view(cache);
+  make_maps(cache, &a.c, &a.maps);
   a.budget = budget;
   a.mode = 2;
   a.capp = 0;
@@ -831,20 +1023,22 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
     return TRI_DISPATCH(run_fused, cache->d, G, bf16, a, units, stream);
   }
   const SplitWs w = split_ws(cache, G);
-  if (ws == nullptr || ws_bytes < w.total) return TRI_ERR_WORKSPACE;
+  if (ws == nullptr || ws_bytes < w.total || !aligned16(ws)) return TRI_ERR_WORKSPACE;
   SCArgs sa;
   std::memset(&sa, 0, sizeof(sa));
   sa.c = make_view(cache);
+  make_maps(cache, &sa.c, &sa.maps);
   sa.G = G;
   sa.budget = params->budget;
   sa.mode = 0;
   sa.ntiles = ntiles_of(cache);
   sa.capp = round32(cache->cap);
   sa.bcap = bcap_of(cache, params->budget);
-  if (SCLayout(sa.capp, sa.bcap).total > kMaxSmem) return TRI_ERR_UNSUPPORTED;
+  if (SCLayout(sa.capp, sa.bcap, 0).total > kMaxSmem) return TRI_ERR_UNSUPPORTED;
   TileArgs ta = tile_args(cache, stats, params);
   ta.skip_small = 1;
   ta.raw = reinterpret_cast<float *>(static_cast<char *>(ws) + w.raw_off);
+  ta.raw_stride = sa.capp;
   ta.part = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.part_off);
   if ((e = TRI_DISPATCH(run_tiles, cache->d, G, bf16, ta, units, stream)) != TRI_OK) return e;
   sa.raw = ta.raw;

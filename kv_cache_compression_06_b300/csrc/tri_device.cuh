@@ -4,17 +4,22 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "../../include/tri.h"
 
 namespace tri {
 
-constexpr int kThreads = 256;                   // CTA size of the score / fused kernels
-constexpr int kWarps = kThreads / 32;
+constexpr int kFusedThreads = 256;             // CTA size of the fused short-unit kernel
+constexpr int kConsumerWarps = 8;              // warps that score keys (long-unit tiles)
+constexpr int kProducerWarp = kConsumerWarps;   // the warp that issues the K loads
+constexpr int kThreads = (kConsumerWarps + 1) * 32;   // CTA size of the long-unit score kernel
 constexpr int kStageBytes = 16384;              // one pipeline stage (K tile or K+V chunk)
-constexpr int kStages = 4;
+constexpr int kStages = 4;                      // stages of the score ring
 constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kMaxCompactStages = 16;           // stages of the compaction ring, at most
 constexpr int kTileKeys = 2048;                 // keys per CTA in the split (long-unit) path
 constexpr int kSelThreads = 512;                // CTA size of the select/compact kernel
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // bounded device waits: 2 s
@@ -86,6 +91,39 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// Tiled 4-D tensor load (TMA) of the box at coordinates (c0, c1, c2, c3) of the
+// tensor map `map` (a kernel parameter) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Tiled 2-D gather (TMA tile::gather4): loads rows r0..r3 (box one row high,
+// `col` the first element) of the 2-D tensor map `map` into four consecutive
+// rows at dst, completing on `bar`.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, int col, int r0, int r1,
+                                            int r2, int r3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Tiled 4-D tensor store (TMA) of the box at (c0, c1, c2, c3) from shared memory,
+// tracked by the issuing thread's bulk async-groups.  Coordinates must be >= 0.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                             const void *src) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+               : "memory");
+}
+
 // shared -> global bulk store, tracked by the issuing thread's bulk async-groups.
 __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
@@ -114,6 +152,12 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Arrives on `bar` once all of this thread's earlier cp.async copies have landed;
+// the arrival counts toward the barrier's expected count (noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
@@ -155,6 +199,18 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
   if (f == 0.0f) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
 }
 
 // ---------------------------------------------------------------- block reductions

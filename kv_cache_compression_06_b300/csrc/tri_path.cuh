@@ -20,6 +20,14 @@ struct StepConst {
   float2 phi[64];
 };
 
+// Tensor maps of one call (kernel parameters, valid per the CacheView flags):
+// k4/v4 view a paged pool as [L*nblocks][block][Hkv][d] with a box of one block
+// of one head; k2/v2 view the K/V storage as rows [rows][d] with a box of one row
+// (for tile::gather4).
+struct TmaMaps {
+  CUtensorMap k4, v4, k2, v2;
+};
+
 // Dense [L][S][Hkv][cap][d] or paged [L][nblocks][block][Hkv][d] addressing.
 struct CacheView {
   char *k;
@@ -30,6 +38,8 @@ struct CacheView {
   const int *bt;          // block table [S][max_blocks] or nullptr
   int max_blocks, block;
   long long nblocks;
+  int tm_ok;              // paged, and the block maps (box = one block of one head) are valid
+  int g4_ok;              // the row maps (2-D [rows][d], box one row) are valid
 
   __device__ __forceinline__ bool paged() const { return bt != nullptr; }
   // Byte offset of slot i of unit (l, s, g); -1 if the block id is out of range.
@@ -39,12 +49,21 @@ struct CacheView {
     if (b < 0 || b >= nblocks) return -1;
     return ((((long long)l * nblocks + b) * block + (i % block)) * Hkv + g) * (long long)rb;
   }
-  // Checks every block id a unit of sequence s with n keys will touch.
-  __device__ bool blocks_ok(int s, int n) const {
+  // Row of slot i of unit (l, s, g) in the 2-D row view [rows][d] of the K/V
+  // storage (dense: u*cap + i; paged: pool row); -1 if the block id is out of range.
+  __device__ __forceinline__ long long row2d(int l, int s, int g, int i) const {
+    if (bt == nullptr) return (((long long)l * S + s) * Hkv + g) * cap + i;
+    const int b = bt[(long long)s * max_blocks + i / block];
+    if (b < 0 || b >= nblocks) return -1;
+    return (((long long)l * nblocks + b) * block + (i % block)) * Hkv + g;
+  }
+  // Checks every block id that rows [row0, row0 + n) of sequence s touch
+  // (CTA-wide; every thread gets the answer).
+  __device__ bool blocks_ok(int s, int n, int row0 = 0) const {
     if (bt == nullptr) return true;
-    const int nb = (n + block - 1) / block;
+    const int b0 = row0 / block, nb = (row0 + n + block - 1) / block;
     int bad = 0;
-    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    for (int b = b0 + threadIdx.x; b < nb; b += blockDim.x) {
       const int id = bt[(long long)s * max_blocks + b];
       bad |= (id < 0 || id >= nblocks);
     }
@@ -190,13 +209,15 @@ __device__ __forceinline__ void load_lane_weights(LaneWeights<G> &lw, const floa
 
 // Scores the rows [0, nrows) of a tile in shared memory; s_{h, row0 + r} goes to
 // scores[h * sstride + row0 + r].  Per lane and head: 6 paired FMAs over its 4
-// bands (Re A * Re k~ + Im A * Im k~ + W * |k~|), then a cross-lane sum.
+// bands (Re A * Re k~ + Im A * Im k~ + W * |k~|), then a cross-lane sum.  Called
+// by the `nw` consumer warps; `warp` is this warp's index among them.
 template <int D, int G, bool BF16>
 __device__ __forceinline__ void score_tile(const char *tile, int nrows, int row0, float *scores,
-                                           int sstride, const LaneWeights<G> &lw, bool inter) {
+                                           int sstride, const LaneWeights<G> &lw, bool inter, int warp,
+                                           int nw) {
   using RG = RowGeom<D, BF16>;
   constexpr int LPR = RG::LPR, RPW = RG::RPW, RB = RG::RB;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int j = lane % LPR;
   const int rsub = lane / LPR;
   const int head = j / (LPR / G);
@@ -236,6 +257,7 @@ __device__ __forceinline__ void score_tile(const char *tile, int nrows, int row0
   }
 }
 
+// ---------------------------------------------------------------- K streaming (short units)
 // Issues the copy of rows [row0, row0 + nrows) of one unit's K into `dst` on
 // `bar` (arrival count 32: every lane of the calling warp arrives once).
 // Dense: one bulk copy of the contiguous rows.  Paged: one bulk copy per row.
@@ -263,6 +285,9 @@ __device__ __forceinline__ void issue_rows(const CacheView &c, int l, int s, int
   }
 }
 
+// Short-unit variant of the K streaming (the fused kernel's): every warp scores,
+// warp 0 refills a stage right after the CTA barrier that ends it.  With two
+// CTAs per SM this measured faster than the producer-warp pipeline below.
 // Streams rows [0, n) of unit (l, s, g) through the ring and scores them into
 // scores[h * sstride + i].  Returns false (CTA-uniform) if a wait timed out.
 // The caller has initialised bars[0..kStages) with count 32 and synchronised.
@@ -271,7 +296,7 @@ __device__ bool score_unit_rows(const CacheView &c, int l, int s, int g, int row
                                 char *ring, uint64_t *bars, float *scores, int sstride,
                                 const LaneWeights<G> &lw, bool inter) {
   constexpr int TR = kStageBytes / RowGeom<D, BF16>::RB;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int ntiles = (n + TR - 1) / TR;
   if (warp == 0) {
     for (int t = 0; t < ntiles && t < kStages; ++t)
@@ -282,7 +307,7 @@ __device__ bool score_unit_rows(const CacheView &c, int l, int s, int g, int row
     const int st = t % kStages;
     const bool ok = mbar_wait(&bars[st], (uint32_t)((t / kStages) & 1));
     score_tile<D, G, BF16>(ring + st * kStageBytes, min(TR, n - t * TR), t * TR, scores, sstride,
-                           lw, inter);
+                           lw, inter, warp, nw);
     if (__syncthreads_or(!ok)) return false;
     if (warp == 0 && t + kStages < ntiles) {
       const int tn = t + kStages;
@@ -291,6 +316,124 @@ __device__ bool score_unit_rows(const CacheView &c, int l, int s, int g, int row
     }
   }
   return true;
+}
+
+// ---------------------------------------------------------------- K streaming pipeline
+// The score phase of a CTA is a producer/consumer pipeline over a ring of
+// kStages shared-memory stages of kStageBytes:
+//   - the producer warp (kProducerWarp) loads stage after stage of K rows with
+//     bulk / tensor copies (TMA), completing on full[st] (arrival count 1 plus the
+//     transaction bytes);
+//   - the kConsumerWarps consumer warps score each stage, then each arrives once
+//     on empty[st] (arrival count kConsumerWarps), which lets the producer
+//     refill it.
+// No block-wide barrier is taken per stage.  Every wait is bounded: a wait that
+// gives up records TRI_ERR_TIMEOUT and sets *fail (shared), the pipeline runs to
+// its end without waiting further on that stage, and the CTA drains its copies
+// in flight (bounded again) before it leaves.
+struct Pipe {
+  char *ring;
+  uint64_t *full;    // [kStages]
+  uint64_t *empty;   // [kStages]
+  volatile int *fail;     // shared flag
+  volatile int *issued;   // shared: stages the producer issued
+};
+
+// Initialises the pipeline barriers (thread 0; caller synchronises).
+__device__ __forceinline__ void pipe_init(const Pipe &p) {
+  for (int st = 0; st < kStages; ++st) {
+    mbar_init(&p.full[st], 1);
+    mbar_init(&p.empty[st], kConsumerWarps);
+  }
+  *p.fail = 0;
+  *p.issued = 0;
+  fence_mbar_init();
+}
+
+// Producer side: loads rows [row0, row0 + nrows) of unit (l, s, g)'s K into dst,
+// completing on `full`.  Dense: one bulk copy of the contiguous rows.  Paged with
+// a tensor map: one 4-D tensor copy per block (box = one block of one head; rows
+// of the last block past nrows are loaded too, they exist).  Paged without: one
+// bulk copy per row.  Called by all 32 lanes of the producer warp.
+template <int RB>
+__device__ __forceinline__ void produce_stage(const CacheView &c, const CUtensorMap *tmk, int l, int s,
+                                              int g, int row0, int nrows, char *dst, uint64_t *full,
+                                              int lane) {
+  if (!c.paged()) {
+    if (lane == 0) {
+      const uint32_t bytes = (uint32_t)nrows * (uint32_t)RB;
+      mbar_arrive_expect_tx(full, bytes);
+      bulk_g2s(dst, c.k + c.row_off(l, s, g, row0), bytes, full);
+    }
+    return;
+  }
+  if (c.tm_ok) {
+    const int blk = c.block, nblk = (nrows + blk - 1) / blk;
+    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nblk * blk * RB));
+    __syncwarp();
+    if (lane < nblk) {
+      const int b = c.bt[(long long)s * c.max_blocks + row0 / blk + lane];
+      tma_load_4d(dst + lane * blk * RB, tmk, 0, g, 0, (int)((long long)l * c.nblocks + b), full);
+    }
+    return;
+  }
+  int bytes = 0;
+  for (int r = lane; r < nrows; r += 32) bytes += (c.row_off(l, s, g, row0 + r) >= 0) ? RB : 0;
+  bytes = warp_sum_int(bytes);
+  if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)bytes);
+  __syncwarp();
+  for (int r = lane; r < nrows; r += 32) {
+    const long long off = c.row_off(l, s, g, row0 + r);
+    if (off >= 0) bulk_g2s(dst + (long long)r * RB, c.k + off, (uint32_t)RB, full);
+  }
+}
+
+// Streams rows [row_begin, row_begin + n) of unit (l, s, g) through the ring and
+// scores them into scores[h * sstride + i] (i relative to row_begin).  Called by
+// every thread of the CTA (kThreads); returns false (CTA-uniform, after a
+// barrier) if a wait gave up.  The caller initialised the pipe and synchronised.
+template <int D, int G, bool BF16>
+__device__ bool stream_and_score(const CacheView &c, const CUtensorMap *tmk, int l, int s, int g,
+                                 int row_begin, int n, const Pipe &p, float *scores, int sstride,
+                                 const LaneWeights<G> &lw, bool inter) {
+  using RG = RowGeom<D, BF16>;
+  constexpr int TR = kStageBytes / RG::RB;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = (n + TR - 1) / TR;
+  if (warp == kProducerWarp) {
+    int t = 0;
+    for (; t < ntiles; ++t) {
+      const int st = t % kStages;
+      if (*p.fail || (t >= kStages && !mbar_wait(&p.empty[st], (uint32_t)(((t / kStages) - 1) & 1)))) {
+        *p.fail = 1;
+        break;
+      }
+      produce_stage<RG::RB>(c, tmk, l, s, g, row_begin + t * TR, min(TR, n - t * TR),
+                            p.ring + st * kStageBytes, &p.full[st], lane);
+    }
+    if (lane == 0) *p.issued = t;
+  } else {
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % kStages;
+      if (!*p.fail && !mbar_wait(&p.full[st], (uint32_t)((t / kStages) & 1))) *p.fail = 1;
+      score_tile<D, G, BF16>(p.ring + st * kStageBytes, min(TR, n - t * TR), t * TR, scores, sstride, lw,
+                             inter, warp, kConsumerWarps);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p.empty[st]);
+    }
+  }
+  __syncthreads();
+  if (*p.fail == 0) return true;
+  // Drain: wait (bounded) for the last phase issued on every stage.
+  if (threadIdx.x == 0) {
+    const int issued = *p.issued;
+    for (int st = 0; st < kStages && st < issued; ++st) {
+      const int last = st + ((issued - 1 - st) / kStages) * kStages;
+      mbar_wait(&p.full[st], (uint32_t)((last / kStages) & 1));
+    }
+  }
+  __syncthreads();
+  return false;
 }
 
 // ---------------------------------------------------------------- GQA moments (a3)
@@ -327,11 +470,18 @@ __device__ __forceinline__ void head_moments(const float *scores, int sstride, i
 }
 
 // ---------------------------------------------------------------- top-B (a4)
+// Shared scratch of the selection (ints): [0..1] radix result, [8..23] per-warp
+// partial sums of the histogram scan, [24..39] per-warp tie counts, [40..55]
+// per-warp kept counts, [56] first dropped slot.  kSelInts ints.
+constexpr int kSelInts = 64;
+
+// Short-unit variant of the selection (the fused kernel's; measured faster there
+// than the variants below, whose extra passes only pay off for long units).
 // Radix select (8-bit digits, most significant first) of the K-th largest key
 // among keys[0..n).  Returns the threshold key T and, in *ntie, how many keys
 // equal to T are kept (the lowest slots).  Needs blockDim >= 256.
 // hist: 256 u32; sm: 4 ints.
-__device__ __noinline__ uint32_t radix_select(const uint32_t *keys, int n, int K, uint32_t *hist,
+__device__ __noinline__ uint32_t radix_select_atomic(const uint32_t *keys, int n, int K, uint32_t *hist,
                                               int *sm, int *ntie) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t prefix = 0, mask = 0;
@@ -381,8 +531,9 @@ __device__ __noinline__ uint32_t radix_select(const uint32_t *keys, int n, int K
 
 // Writes the kept slots of keys[0..n) (those > T, plus the first ntie equal to
 // T in slot order) to idx[0..K) in ascending order; returns the first dropped
-// slot (n if none).  Never writes past idx[K-1].  sm: 40 ints.
-__device__ __noinline__ int build_kept(const uint32_t *keys, int n, int K, uint32_t T, int ntie,
+// slot (n if none).  Never writes past idx[K-1].  Each thread walks a
+// contiguous chunk of slots.  sm: 40 ints.
+__device__ __noinline__ int build_kept_chunked(const uint32_t *keys, int n, int K, uint32_t T, int ntie,
                                        int *idx, int *sm) {
   const int tid = threadIdx.x;
   const int chunk = (n + blockDim.x - 1) / blockDim.x;
@@ -423,10 +574,146 @@ __device__ __noinline__ int build_kept(const uint32_t *keys, int n, int K, uint3
   return e0;
 }
 
+// Adds one key per lane (where `valid`) to the histogram of its top byte
+// (the first radix digit).  A score distribution puts most keys into a handful
+// of top bytes, so the lanes of a warp are grouped by digit (ballot per
+// distinct digit) and each group adds its count with one atomic.  Warp-uniform.
+__device__ __forceinline__ void hist_add_top(uint32_t *hist, uint32_t key, bool valid) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t d = key >> 24;
+  unsigned todo = __ballot_sync(0xffffffffu, valid);
+  while (todo != 0u) {
+    const int leader = __ffs(todo) - 1;
+    const uint32_t dl = __shfl_sync(0xffffffffu, d, leader);
+    const unsigned same = __ballot_sync(0xffffffffu, valid && d == dl);
+    if (lane == leader) atomicAdd(&hist[dl], (uint32_t)__popc(same));
+    todo &= ~same;
+  }
+}
+
+// Radix select (8-bit digits, most significant first) of the K-th largest key
+// among keys[0..n).  Returns the threshold key T and, in *ntie, how many keys
+// equal to T are kept (the lowest slots).  If `top_ready`, hist already holds
+// the histogram of the top byte over all n keys (built by hist_add_top while
+// the keys were written) and the first pass only selects.  Needs 256 <=
+// blockDim <= 512, a multiple of 32.  hist: 256 u32.
+__device__ __noinline__ uint32_t radix_select(const uint32_t *keys, int n, int K, uint32_t *hist,
+                                              int *sm, int *ntie, bool top_ready) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+  uint32_t prefix = 0, mask = 0;
+  int k = K;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    if (shift < 24 || !top_ready) {
+      for (int b = tid; b < 256; b += nt) hist[b] = 0;
+      __syncthreads();
+      if (shift == 24) {
+        for (int base = tid & ~31; base < n; base += nt) {
+          const int i = base + lane;
+          hist_add_top(hist, i < n ? keys[i] : 0u, i < n);
+        }
+      } else {
+        for (int i = tid; i < n; i += nt) {
+          const uint32_t u = keys[i];
+          if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        }
+      }
+    }
+    __syncthreads();
+    // Suffix counts S[x] = #{digit >= x}: thread t < 256 scans the reversed
+    // histogram, so its inclusive prefix P_t equals S[255 - t] and P_{t-1}
+    // equals S[256 - t].  The digit x is the one with S[x] >= k > S[x + 1].
+    int P = 0, wsum = 0;
+    if (tid < 256) {
+      P = (int)hist[255 - tid];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, P, o);
+        if (lane >= o) P += y;
+      }
+      if (lane == 31) sm[8 + warp] = P;
+    }
+    __syncthreads();
+    if (tid < 256) {
+      for (int w = 0; w < warp; ++w) wsum += sm[8 + w];
+      P += wsum;
+      int Pprev = __shfl_up_sync(0xffffffffu, P, 1);
+      if (lane == 0) Pprev = wsum;
+      if (P >= k && Pprev < k) {
+        sm[0] = 255 - tid;
+        sm[1] = k - Pprev;
+      }
+    }
+    __syncthreads();
+    const uint32_t dgt = (uint32_t)sm[0];
+    k = sm[1];
+    prefix |= dgt << shift;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  *ntie = k;
+  return prefix;
+}
+
+// Writes the kept slots of keys[0..n) (those > T, plus the first ntie equal to
+// T in slot order) to idx[0..K) in ascending order; returns the first dropped
+// slot (n if none).  Never writes past idx[K-1].  Each warp owns one contiguous
+// segment of slots and walks it 32 consecutive slots at a time (ballot + popc
+// for the in-order positions), so lanes read consecutive words.
+__device__ __noinline__ int build_kept(const uint32_t *keys, int n, int K, uint32_t T, int ntie,
+                                       int *idx, int *sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int seg = (((n + nw - 1) / nw) + 31) / 32 * 32;
+  const int lo = min(n, warp * seg), hi = min(n, lo + seg);
+  int cgt = 0, ceq = 0;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const uint32_t u = i < hi ? keys[i] : 0u;
+    cgt += __popc(__ballot_sync(0xffffffffu, i < hi && u > T));
+    ceq += __popc(__ballot_sync(0xffffffffu, i < hi && u == T));
+  }
+  if (lane == 0) {
+    sm[24 + warp] = ceq;
+    sm[40 + warp] = cgt;
+  }
+  if (tid == 0) sm[56] = n;
+  __syncthreads();
+  int eq_before = 0, kept_before = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int e = sm[24 + w];
+    const int tw = max(0, min(e, ntie - eq_before));
+    kept_before += sm[40 + w] + tw;
+    eq_before += e;
+  }
+  const unsigned lt = lanemask_lt();
+  int eq_run = eq_before, pos_run = kept_before, first_drop = n;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < hi;
+    const uint32_t u = valid ? keys[i] : 0u;
+    const unsigned eqm = __ballot_sync(0xffffffffu, valid && u == T);
+    const bool keep = valid && (u > T || (u == T && eq_run + __popc(eqm & lt) < ntie));
+    const unsigned km = __ballot_sync(0xffffffffu, keep);
+    const unsigned dm = __ballot_sync(0xffffffffu, valid && !keep);
+    const int pos = pos_run + __popc(km & lt);
+    if (keep && pos < K) idx[pos] = i;
+    if (dm != 0u && first_drop == n) first_drop = base + __ffs(dm) - 1;
+    eq_run += __popc(eqm);
+    pos_run += __popc(km);
+  }
+  if (lane == 0 && first_drop < n) atomicMin(&sm[56], first_drop);
+  __syncthreads();
+  const int e0 = sm[56];
+  __syncthreads();
+  return e0;
+}
+
 // ---------------------------------------------------------------- compaction (a5)
-// In-place ordered gather of K and V rows of unit (l, s, g): row j <- row idx[j]
-// for j in [e0, B) (rows below e0 are kept in place), executed by warp 0 alone
-// with bulk (TMA) copies; the other warps may leave.
+// Short-unit variant of the compaction (the fused kernel's): warp 0 alone, bulk
+// copies only, a fixed ring of kStages stages.  Its per-chunk issue path is the
+// shortest dependency chain, which is what bounds a single warp moving ~2000
+// mostly contiguous rows.  In-place ordered gather of K and V rows of unit
+// (l, s, g): row j <- row idx[j] for j in [e0, B) (rows below e0 are kept in
+// place); the other warps may leave.
 //
 // Destination chunks of up to 32 rows (K and V, one ring stage) are processed in
 // ascending order.  Lane r of warp 0 owns destination row j0 + r of a chunk.
@@ -441,7 +728,7 @@ __device__ __noinline__ int build_kept(const uint32_t *keys, int n, int K, uint3
 //
 // cbars: kStages mbarriers initialised with arrival count 1.  Returns false if a
 // wait timed out (status recorded).
-__device__ __noinline__ bool compact_unit_tma(const CacheView &c, int l, int s, int g,
+__device__ __noinline__ bool compact_unit_runs(const CacheView &c, int l, int s, int g,
                                               const int *idx, int e0, int B, int N, char *ring,
                                               uint64_t *cbars) {
   const int lane = threadIdx.x & 31;
@@ -516,6 +803,167 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, int l, int s, 
     bulk_wait_read<1>();   // the stores of chunk cidx-1 no longer read their stage
     __syncwarp();
     if (cidx + kStages - 1 < nch) issue_loads(cidx + kStages - 1);   // refills that stage
+  }
+  bulk_wait<0>();
+  return ok;
+}
+
+// In-place ordered gather of K and V rows of unit (l, s, g): row j <- row idx[j]
+// for j in [e0, B) (rows below e0 are kept in place), issued by warp 0 alone
+// with TMA copies; the other warps may leave.
+//
+// Destination chunks of ch rows (K rows then V rows fill one ring stage; lane r
+// owns destination row j0 + r) are processed in ascending order.
+// Loads, per chunk and tensor (a TMA op costs tens of ns to issue, so the
+// number of ops per chunk is what is minimised):
+//   - dense caches whose chunk has at most kRunLimit runs of consecutive source
+//     slots: one bulk copy per run;
+//   - otherwise (scattered sources, and every chunk of a paged cache): one
+//     tile::gather4 of 4 source rows per quad of destination rows, through the
+//     row map.
+// Stores: dense, one bulk store per tensor (the destination rows are
+// contiguous); paged with block maps, one tensor store per destination block
+// (chunks then start at a block boundary: rows below e0 in the first block are
+// reloaded from themselves and rewritten unchanged; rows at or past B in the
+// last block receive don't-care values); otherwise one bulk store per row.
+// In-place safety: a chunk is stored only after its loads completed, and every
+// load of a later chunk reads slots >= that chunk's first destination, which no
+// earlier store touches, since idx is strictly increasing (idx_j >= j).  A ring
+// stage is refilled only after the bulk stores that read it finished reading.
+//
+// ring: nstages (2..kMaxCompactStages) stages of kStageBytes; cbars: nstages
+// mbarriers initialised with arrival count 1.  Returns false if a wait timed out
+// (status recorded; loads already issued are waited for, bounded).
+constexpr int kRunLimit = 8;   // runs per chunk up to which bulk copies beat gather4
+
+__device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps *maps, int l, int s, int g,
+                                              const int *idx, int e0, int B, int N, char *ring,
+                                              int nstages, uint64_t *cbars) {
+  const int lane = threadIdx.x & 31;
+  const int rb = c.rb;
+  const int ch = min(32, kStageBytes / (2 * rb));   // rows per chunk (a multiple of 4)
+  if (B - e0 <= 0) return true;
+  const bool paged = c.paged();
+  const bool blkst = paged && c.tm_ok && ch % c.block == 0;
+  const int jb = blkst ? (e0 / c.block) * c.block : e0;
+  const int nch = (B - jb + ch - 1) / ch;
+
+  auto issue_loads = [&](int cidx) {
+    const int st = cidx % nstages;
+    char *sk = ring + st * kStageBytes;   // K rows [0, ch), then V rows [ch, 2ch)
+    const int j0 = jb + cidx * ch;
+    const int rows = min(ch, B - j0);
+    int src = -1;
+    bool valid = lane < rows;
+    if (valid) {
+      src = idx[j0 + lane];
+      if (src < 0 || src >= N) {
+        set_status(TRI_ERR_BOUNDS);
+        valid = false;
+      }
+    }
+    const long long r2 = valid ? c.row2d(l, s, g, src) : -1;
+    if (r2 < 0) valid = false;
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    // runs of consecutive source slots (dense caches only: paged rows of one
+    // head are not adjacent in memory)
+    const int prev = __shfl_up_sync(0xffffffffu, src, 1);
+    const bool boundary = valid && (paged || lane == 0 || !((vmask >> (lane - 1)) & 1u) || prev + 1 != src);
+    const unsigned bmask = __ballot_sync(0xffffffffu, boundary);
+    const bool use_runs = !paged && (__popc(bmask) <= kRunLimit || c.g4_ok == 0);
+    int bytes = 0;
+    if (use_runs) {
+      // one bulk copy per run [lane, next boundary or invalid lane)
+      if (boundary) {
+        const unsigned stop = (bmask | ~vmask) & (lane == 31 ? 0u : (0xffffffffu << (lane + 1)));
+        const int end = stop ? (__ffs(stop) - 1) : 32;
+        bytes = (end - lane) * rb;
+      }
+      bytes = 2 * warp_sum_int(bytes);
+      if (lane == 0) mbar_arrive_expect_tx(&cbars[st], (uint32_t)bytes);
+      __syncwarp();
+      if (boundary) {
+        const unsigned stop = (bmask | ~vmask) & (lane == 31 ? 0u : (0xffffffffu << (lane + 1)));
+        const int end = stop ? (__ffs(stop) - 1) : 32;
+        const long long off = r2 * rb;
+        bulk_g2s(sk + (long long)lane * rb, c.k + off, (uint32_t)((end - lane) * rb), &cbars[st]);
+        bulk_g2s(sk + (long long)(ch + lane) * rb, c.v + off, (uint32_t)((end - lane) * rb), &cbars[st]);
+      }
+    } else if (c.g4_ok) {
+      // one tile::gather4 per quad of destination rows (lanes past `rows`
+      // repeat the quad's first valid row; those smem rows are never stored)
+      const int q0 = lane & ~3;
+      const unsigned qmask = 0xfu << q0;
+      const int firstv = __ffs(vmask & qmask) - 1;
+      const long long rfill = __shfl_sync(0xffffffffu, r2, firstv < 0 ? lane : firstv);
+      const int rc = (int)(valid ? r2 : rfill);
+      const int c0 = __shfl_sync(0xffffffffu, rc, q0);
+      const int c1 = __shfl_sync(0xffffffffu, rc, q0 + 1);
+      const int c2 = __shfl_sync(0xffffffffu, rc, q0 + 2);
+      const int c3 = __shfl_sync(0xffffffffu, rc, q0 + 3);
+      const bool gath = lane == q0 && (vmask & qmask) != 0u;
+      bytes = 2 * warp_sum_int(gath ? 4 * rb : 0);
+      if (lane == 0) mbar_arrive_expect_tx(&cbars[st], (uint32_t)bytes);
+      __syncwarp();
+      if (gath) {
+        tma_gather4(sk + (long long)q0 * rb, &maps->k2, 0, c0, c1, c2, c3, &cbars[st]);
+        tma_gather4(sk + (long long)(ch + q0) * rb, &maps->v2, 0, c0, c1, c2, c3, &cbars[st]);
+      }
+    } else {
+      // paged without row maps: one bulk copy per row
+      bytes = 2 * warp_sum_int(valid ? rb : 0);
+      if (lane == 0) mbar_arrive_expect_tx(&cbars[st], (uint32_t)bytes);
+      __syncwarp();
+      if (valid) {
+        const long long off = r2 * rb;
+        bulk_g2s(sk + (long long)lane * rb, c.k + off, (uint32_t)rb, &cbars[st]);
+        bulk_g2s(sk + (long long)(ch + lane) * rb, c.v + off, (uint32_t)rb, &cbars[st]);
+      }
+    }
+  };
+
+  for (int x = 0; x < nstages - 1 && x < nch; ++x) issue_loads(x);
+  bool ok = true;
+  int cidx = 0;
+  for (; cidx < nch; ++cidx) {
+    const int st = cidx % nstages;
+    const char *sk = ring + st * kStageBytes;
+    const int j0 = jb + cidx * ch;
+    const int rows = min(ch, B - j0);
+    if (!mbar_wait(&cbars[st], (uint32_t)((cidx / nstages) & 1))) {
+      ok = false;
+      break;
+    }
+    if (!paged) {
+      if (lane == 0) {
+        const long long off = c.row_off(l, s, g, j0);
+        bulk_s2g(c.k + off, sk, (uint32_t)(rows * rb));
+        bulk_s2g(c.v + off, sk + (long long)ch * rb, (uint32_t)(rows * rb));
+      }
+    } else if (blkst) {
+      const int nb = (rows + c.block - 1) / c.block;
+      if (lane < nb) {
+        const int b = c.bt[(long long)s * c.max_blocks + j0 / c.block + lane];
+        const int z = (int)((long long)l * c.nblocks + b);
+        tma_store_4d(&maps->k4, 0, g, 0, z, sk + (long long)lane * c.block * rb);
+        tma_store_4d(&maps->v4, 0, g, 0, z, sk + (long long)(ch + lane * c.block) * rb);
+      }
+    } else if (lane < rows) {
+      const long long off = c.row_off(l, s, g, j0 + lane);
+      if (off >= 0) {
+        bulk_s2g(c.k + off, sk + (long long)lane * rb, (uint32_t)rb);
+        bulk_s2g(c.v + off, sk + (long long)(ch + lane) * rb, (uint32_t)rb);
+      }
+    }
+    bulk_commit();
+    bulk_wait_read<1>();   // the stores of chunk cidx-1 no longer read their stage
+    __syncwarp();
+    if (cidx + nstages - 1 < nch) issue_loads(cidx + nstages - 1);   // refills that stage
+  }
+  if (!ok) {
+    // loads of chunks [cidx, cidx + nstages - 1) may still be in flight
+    for (int x = cidx; x < nch && x < cidx + nstages - 1; ++x)
+      if (!mbar_wait(&cbars[x % nstages], (uint32_t)((x / nstages) & 1))) break;
   }
   bulk_wait<0>();
   return ok;
