@@ -48,7 +48,8 @@
  *     range, an idx list that is not strictly increasing inside [0, N)) skip the
  *     affected unit and record the first error code in a device status word read
  *     by tri_get_device_status().  Device waits are bounded; a wait that gives
- *     up records TRI_ERR_TIMEOUT.
+ *     up records TRI_ERR_TIMEOUT, after which the kernels of this and later calls
+ *     return without work until tri_clear_device_status().
  *   - No C++ exception crosses this ABI.
  */
 #ifndef TRI_H

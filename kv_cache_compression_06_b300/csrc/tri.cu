@@ -21,7 +21,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "tri_path.cuh"
+#include "tri_mma.cuh"
 
 namespace tri {
 
@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kFusedThreads, (G <= 4 ? 2 : 1)) fused_kernel(
   const int tid = threadIdx.x, nt = blockDim.x;
   const int u = blockIdx.x;
   const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
+  if (timed_out()) return;
   const int N = c.seq_len[s];
   const int B = a.budget;
   if (N < 0 || N > c.cap) {
@@ -218,19 +219,21 @@ __device__ __forceinline__ Pipe make_pipe(char *smem, int bars) {
 
 // ---------------------------------------------------------------- long units: tiles
 struct TileArgs {
-  TmaMaps maps;      // as in FusedArgs (k4 only is used)
+  TmaMaps maps;      // k4 (CUDA-core variant)
+  CUtensorMap ks;    // tensor-core variant: 128B-swizzled K map (dense 2-D, paged 4-D), boxes of 64 elements
   CacheView c;
   const float *center, *R, *mag;
   int Hq;
   const int *t;
-  int budget, skip_small, inter, ntiles;
+  int budget, skip_small, inter, ntiles, mma_ok;
   long long raw_stride;   // floats between the raw rows of two heads (cap, or capp in the workspace)
   float *raw;      // [(u*G + h)*raw_stride + i]
   float2 *part;    // [(u*ntiles + tile)*G + h] = (mean, M2) of the tile
   StepConst sc;
 };
 
-constexpr int kTileStride = kTileKeys + 4;   // per-head score stride (= 4 mod 32: no bank conflicts)
+// per-head score stride of a tile (= 4 mod 32: no bank conflicts)
+__host__ __device__ constexpr int tile_stride_for(int G) { return tile_keys_for(G) + 4; }
 
 struct TileLayout {
   int bars, wts, red, scores, total;
@@ -239,31 +242,39 @@ struct TileLayout {
     bars = o;   o += 128;
     wts = o;    o += align_up(G * 3 * F * 4, 128);
     red = o;    o += 512;
-    scores = o; o += G * kTileStride * 4;
+    scores = o; o += G * tile_stride_for(G) * 4;
     total = o;
   }
 };
 
+// Mean and M2 (sum of squared deviations) per head over one tile's scores,
+// two passes, on the scores minus the tile's first score (as head_moments): a
+// constant tile gets M2 = 0 exactly and its mean equals the constant.
 template <int G>
 __device__ __forceinline__ void head_mean_m2(const float *scores, int stride, int n, float *red,
                                              float (&mu)[G], float (&m2)[G]) {
-  float v[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) v[h] = 0.f;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) v[h] += scores[h * stride + i];
-  }
-  block_sum<G>(v, red);
+  float v[G], sh[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    mu[h] = v[h] / (float)n;
+    v[h] = 0.f;
+    sh[h] = scores[h * stride];
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) v[h] += scores[h * stride + i] - sh[h];
+  }
+  block_sum<G>(v, red);
+  float md[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    md[h] = v[h] / (float)n;
+    mu[h] = sh[h] + md[h];
     v[h] = 0.f;
   }
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float dl = scores[h * stride + i] - mu[h];
+      const float dl = (scores[h * stride + i] - sh[h]) - md[h];
       v[h] = fmaf(dl, dl, v[h]);
     }
   }
@@ -286,15 +297,17 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   const int tid = threadIdx.x, nt = blockDim.x;
   const int tile = blockIdx.x, u = blockIdx.y;
   const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
+  if (timed_out()) return;
   const int N = c.seq_len[s];
   if (N < 0 || N > c.cap) {
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
   if (a.skip_small && N <= a.budget) return;
-  const int i0 = tile * kTileKeys;
+  constexpr int TK = tile_keys_for(G), TS = tile_stride_for(G);
+  const int i0 = tile * TK;
   if (i0 >= N) return;
-  const int n = min(kTileKeys, N - i0);
+  const int n = min(TK, N - i0);
   if (!c.blocks_ok(s, n, i0)) {
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
@@ -304,15 +317,143 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   __syncthreads();
   LaneWeights<G> lw;
   load_lane_weights<G, F>(lw, wts, (tid & 31) % RowGeom<D, BF16>::LPR);
-  if (!stream_and_score<D, G, BF16>(c, &a.maps.k4, l, s, g, i0, n, pipe, scores, kTileStride, lw,
+  if (!stream_and_score<D, G, BF16>(c, &a.maps.k4, l, s, g, i0, n, pipe, scores, TS, lw,
                                     a.inter != 0))
     return;
   for (int i = tid; i < n; i += nt) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * a.raw_stride + i0 + i] = scores[h * kTileStride + i];
+    for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * a.raw_stride + i0 + i] = scores[h * TS + i];
   }
   float mu[G], m2[G];
-  head_mean_m2<G>(scores, kTileStride, n, red, mu, m2);
+  head_mean_m2<G>(scores, TS, n, red, mu, m2);
+  if (tid == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      a.part[((long long)u * a.ntiles + tile) * G + h] = make_float2(mu[h], m2[h]);
+  }
+}
+
+// Loads rows [row0, row0 + nrows) of unit (l, s, g)'s K into a swizzled stage
+// of kStageBytes (two boxes of 64 elements per row for d = 128, one for d = 64).
+// Dense: the unit's slot 0 is row urow0 of the 2-D view; rows past the unit are
+// loaded too and never scored, rows past the tensor read as zero.  Paged: one
+// copy per block and half.  Called by all lanes of the producer warp.
+template <int D>
+__device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUtensorMap *map, int l, int s, int g,
+                                                 long long urow0, int row0, int nrows, char *dst, uint64_t *full,
+                                                 int lane) {
+  constexpr int TR = kStageBytes / (2 * D), NH = D / 64;   // rows per stage, halves per row
+  if (!c.paged()) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(full, (uint32_t)kStageBytes);
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) tma_load_2d(dst + hh * TR * 128, map, 64 * hh, (int)(urow0 + row0), full);
+    }
+    return;
+  }
+  const int blk = c.block, nblk = (nrows + blk - 1) / blk;
+  if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nblk * blk * 128 * NH));
+  __syncwarp();
+  if (lane < nblk) {
+    const int b = c.bt[(long long)s * c.max_blocks + row0 / blk + lane];
+    const int z = (int)((long long)l * c.nblocks + b);
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) tma_load_4d(dst + hh * TR * 128 + lane * blk * 128, map, 64 * hh, g, 0, z, full);
+  }
+}
+
+// Tensor-core variant of score_tiles_kernel for bf16 caches with rotate-half
+// bands: each stage of TR rows holds TR / 16 key tiles of 16, which the
+// consumer warps score with score_tile_mma (for d = 128 two groups of 4 warps
+// take alternate stages; the empty barrier then counts the 4 warps of a group).
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __grid_constant__ TileArgs a) {
+  constexpr int F = D / 2;
+  constexpr int TR = kStageBytes / (2 * D);
+  constexpr int SPS = TR / 16;                    // key tiles per stage
+  constexpr int GROUPS = kConsumerWarps / SPS;    // warp groups taking alternate stages
+  extern __shared__ __align__(1024) char smem[];
+  const TileLayout lay(G, F);
+  const Pipe pipe = make_pipe(smem, lay.bars);
+  float *wts = reinterpret_cast<float *>(smem + lay.wts);
+  float *red = reinterpret_cast<float *>(smem + lay.red);
+  float *scores = reinterpret_cast<float *>(smem + lay.scores);
+  const CacheView &c = a.c;
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = blockIdx.x, u = blockIdx.y;
+  const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
+  if (timed_out()) return;
+  const int N = c.seq_len[s];
+  if (N < 0 || N > c.cap) {
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  if (a.skip_small && N <= a.budget) return;
+  constexpr int TK = tile_keys_for(G), TS = tile_stride_for(G);
+  const int i0 = tile * TK;
+  if (i0 >= N) return;
+  const int n = min(TK, N - i0);
+  if (!c.blocks_ok(s, n, i0)) {
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&pipe.full[st], 1);
+      mbar_init(&pipe.empty[st], SPS);
+    }
+    *pipe.fail = 0;
+    *pipe.issued = 0;
+    fence_mbar_init();
+  }
+  build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc);
+  __syncthreads();
+  const int ntiles = (n + TR - 1) / TR;
+  const long long urow0 = (long long)u * c.cap;   // dense: row of slot 0 in the 2-D view
+  if (warp == kProducerWarp) {
+    int t = 0;
+    for (; t < ntiles; ++t) {
+      const int st = t % kStages;
+      if (*pipe.fail || (t >= kStages && !mbar_wait(&pipe.empty[st], (uint32_t)(((t / kStages) - 1) & 1)))) {
+        *pipe.fail = 1;
+        break;
+      }
+      produce_stage_sw<D>(c, &a.ks, l, s, g, urow0, i0 + t * TR, min(TR, n - t * TR),
+                          pipe.ring + st * kStageBytes, &pipe.full[st], lane);
+    }
+    if (lane == 0) *pipe.issued = t;
+  } else {
+    MmaWeights<D, G> w;
+    load_mma_weights<D, G>(w, wts);
+    const int grp = warp / SPS, sub = warp % SPS;
+    const uint32_t ring = smem_u32(pipe.ring);
+    for (int t = grp; t < ntiles; t += GROUPS) {
+      const int st = t % kStages;
+      if (!*pipe.fail && !mbar_wait(&pipe.full[st], (uint32_t)((t / kStages) & 1))) *pipe.fail = 1;
+      score_tile_mma<D, G, TR>(ring + st * kStageBytes, 16 * sub, min(TR, n - t * TR), t * TR, scores,
+                               TS, w);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pipe.empty[st]);
+    }
+  }
+  __syncthreads();
+  if (*pipe.fail) {
+    if (tid == 0) {
+      const int issued = *pipe.issued;
+      for (int st = 0; st < kStages && st < issued; ++st) {
+        const int last = st + ((issued - 1 - st) / kStages) * kStages;
+        mbar_wait(&pipe.full[st], (uint32_t)((last / kStages) & 1));
+      }
+    }
+    __syncthreads();
+    return;
+  }
+  for (int i = tid; i < n; i += nt) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * a.raw_stride + i0 + i] = scores[h * TS + i];
+  }
+  float mu[G], m2[G];
+  head_mean_m2<G>(scores, TS, n, red, mu, m2);
   if (tid == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h)
@@ -344,11 +485,12 @@ __device__ __forceinline__ void merge_tile_moments(const float2 *part, long long
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= G) return;
   const int h = warp;
-  const int used = (N + kTileKeys - 1) / kTileKeys;
+  const int TK = tile_keys_for(G);
+  const int used = (N + TK - 1) / TK;
   float n = 0.f, mean = 0.f, M2 = 0.f;
   for (int t = lane; t < used; t += 32) {
     const float2 p = part[(u * ntiles + t) * G + h];
-    chan_merge(n, mean, M2, (float)min(kTileKeys, N - t * kTileKeys), p.x, p.y);
+    chan_merge(n, mean, M2, (float)min(TK, N - t * TK), p.x, p.y);
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
@@ -387,11 +529,11 @@ __global__ void __launch_bounds__(256) zmax_kernel(const ZArgs a) {
   const int s = (u / a.Hkv) % a.S;
   const int N = a.seq_len[s];
   if (N < 0 || N > a.cap) return;
-  const int i0 = tile * kTileKeys;
+  const int i0 = tile * tile_keys_for(a.G);
   if (i0 >= N) return;
   merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom);
   __syncthreads();
-  const int i1 = min(N, i0 + kTileKeys);
+  const int i1 = min(N, i0 + tile_keys_for(a.G));
   for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
     float z = -INFINITY;
     for (int h = 0; h < a.G; ++h) {
@@ -414,17 +556,19 @@ struct SCArgs {
   int *idx_out, *new_len;
 };
 
-// The keys region follows the ring directly: once the kept list is built the
-// keys are dead and the compaction ring extends over them (nstages stages).
-// A compaction-only launch (capp = 0) reserves `extra` bytes there instead.
+// The keys (one u32 per slot) and the compaction ring share one region at the
+// start of shared memory: the keys are dead once the kept list is built, and
+// the ring is first used after that.  The region holds at least kCompactStages
+// stages (more when the keys need it, up to kMaxCompactStages).
 struct SCLayout {
   int keys, bars, hist, sm, mom, idx, nstages, total;
-  __host__ __device__ SCLayout(int capp, int bcap, int extra) {
-    int o = kRingBytes;
+  __host__ __device__ SCLayout(int capp, int bcap) {
+    int o = 0;
     keys = o;
-    const int kb = align_up(capp * 4 > extra ? capp * 4 : extra, 128);
+    const int kb = align_up(capp * 4 > kCompactStages * kStageBytes ? capp * 4 : kCompactStages * kStageBytes,
+                            kStageBytes);
     o += kb;
-    nstages = min(kMaxCompactStages, (kRingBytes + kb) / kStageBytes);
+    nstages = min(kMaxCompactStages, kb / kStageBytes);
     bars = o; o += kMaxCompactStages * 8;
     hist = o; o += 1024;
     sm = o;   o += kSelInts * 4;
@@ -434,7 +578,7 @@ struct SCLayout {
   }
 };
 
-constexpr int kCompactOnlyExtra = 2 * kRingBytes;   // compaction-only ring: 12 stages
+
 
 // a3 for one long unit from its raw scores: the G rows raw[h][0..N) (stride
 // capp floats, 16-byte aligned) are read with 16-byte loads, U*G of them in
@@ -494,7 +638,7 @@ __device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *
 
 __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __grid_constant__ SCArgs a) {
   extern __shared__ __align__(1024) char smem[];
-  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap, a.mode == 2 ? kCompactOnlyExtra : 0);
+  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap);
   char *ring = smem;
   uint64_t *cbars = reinterpret_cast<uint64_t *>(smem + lay.bars);
   uint32_t *hist = reinterpret_cast<uint32_t *>(smem + lay.hist);
@@ -506,6 +650,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
   const int u = blockIdx.x;
   const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
+  if (timed_out()) return;
   const int N = c.seq_len[s];
   const int B = a.budget;
   if (N < 0 || N > c.cap) {
@@ -706,6 +851,41 @@ static bool make_row_map(const tri_cache *c, void *base, CUtensorMap *map) {
   return r == CUDA_SUCCESS;
 }
 
+// 128B-swizzled K map for the tensor-core score kernel (bf16, rotate-half, d in
+// {64, 128}): dense, a 2-D view [rows][d] with boxes of 64 elements x one
+// stage of rows; paged, the 4-D pool view with boxes of 64 elements x one block
+// of one head (a stage must hold a whole number of blocks, at most 32).
+static bool make_swizzled_map(const tri_cache *c, const tri_params *p, CUtensorMap *map) {
+  if (c->dtype != TRI_BF16 || p->pairing != TRI_PAIR_HALF || (c->d != 64 && c->d != 128)) return false;
+  const int rb = c->d * 2, tr = kStageBytes / rb;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr || c->k == nullptr) return false;
+  CUresult r;
+  if (c->block_table == nullptr) {
+    const int64_t rows = (int64_t)c->L * c->S * c->Hkv * c->cap;
+    if (rows >= (1ll << 31)) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)c->d, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)rb};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)tr};
+    const cuuint32_t estr[2] = {1u, 1u};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->k, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    if (c->block > 256 || tr % c->block != 0 || tr / c->block > 32) return false;
+    if ((int64_t)c->L * c->nblocks >= (1ll << 31)) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)c->d, (cuuint64_t)c->Hkv, (cuuint64_t)c->block,
+                                (cuuint64_t)c->L * (cuuint64_t)c->nblocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)rb, (cuuint64_t)c->Hkv * rb, (cuuint64_t)c->block * c->Hkv * rb};
+    const cuuint32_t box[4] = {64u, 1u, (cuuint32_t)c->block, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, c->k, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS;
+}
+
 // Builds the tensor maps of a call and sets the view's flags.  K and V maps
 // are made together; a V map is needed only when V is given (compaction).
 static void make_maps(const tri_cache *c, CacheView *v, TmaMaps *m) {
@@ -733,7 +913,9 @@ static StepConst make_const(const tri_params *p, int d) {
 
 static int round32(int64_t x) { return (int)((x + 31) / 32 * 32); }
 static int64_t units_of(const tri_cache *c) { return (int64_t)c->L * c->S * c->Hkv; }
-static int ntiles_of(const tri_cache *c) { return (int)((c->cap + kTileKeys - 1) / kTileKeys); }
+static int ntiles_of(const tri_cache *c, int G) {
+  return (int)((c->cap + tile_keys_for(G) - 1) / tile_keys_for(G));
+}
 static bool fused_fits(const tri_cache *c, int G) {
   return FusedLayout(G, c->d / 2, round32(c->cap)).total <= kMaxSmem;
 }
@@ -745,7 +927,7 @@ static SplitWs split_ws(const tri_cache *c, int G) {
   SplitWs w;
   // raw rows padded to round32(cap) floats: 16-byte aligned for bulk copies
   const size_t raw = (size_t)units_of(c) * G * (size_t)round32(c->cap) * sizeof(float);
-  const size_t part = (size_t)units_of(c) * ntiles_of(c) * G * sizeof(float2);
+  const size_t part = (size_t)units_of(c) * ntiles_of(c, G) * G * sizeof(float2);
   w.raw_off = 0;
   w.part_off = (raw + 255) / 256 * 256;
   w.total = w.part_off + (part + 255) / 256 * 256;
@@ -775,6 +957,14 @@ static tri_status run_fused(const FusedArgs &a, int64_t units, cudaStream_t st) 
 template <int D, int G, bool BF16>
 static tri_status run_tiles(const TileArgs &a, int64_t units, cudaStream_t st) {
   const TileLayout lay(G, D / 2);
+  if constexpr (BF16) {
+    if (a.mma_ok) {
+      auto k = score_tiles_mma_kernel<D, G>;
+      if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
+      k<<<dim3((unsigned)a.ntiles, (unsigned)units), kThreads, lay.total, st>>>(a);
+      return launch_result();
+    }
+  }
   auto k = score_tiles_kernel<D, G, BF16>;
   if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
   k<<<dim3((unsigned)a.ntiles, (unsigned)units), kThreads, lay.total, st>>>(a);
@@ -806,7 +996,7 @@ static tri_status run_tiles(const TileArgs &a, int64_t units, cudaStream_t st) {
   }()
 
 static tri_status run_select_compact(const SCArgs &a, int64_t units, cudaStream_t st) {
-  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap, a.mode == 2 ? kCompactOnlyExtra : 0);
+  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap);
   if (lay.total > kMaxSmem) return TRI_ERR_UNSUPPORTED;
   if (set_smem(select_compact_kernel, lay.total) != TRI_OK) return TRI_ERR_CUDA;
   select_compact_kernel<<<(unsigned)units, kSelThreads, lay.total, st>>>(a);
@@ -840,9 +1030,10 @@ static TileArgs tile_args(const tri_cache *c, const tri_stats *stt, const tri_pa
   a.t = p->t;
   a.budget = p->budget;
   a.inter = p->pairing == TRI_PAIR_INTERLEAVED;
-  a.ntiles = ntiles_of(c);
+  a.ntiles = ntiles_of(c, stt->Hq / c->Hkv);
   a.sc = make_const(p, c->d);
   make_maps(c, &a.c, &a.maps);
+  a.mma_ok = make_swizzled_map(c, p, &a.ks) ? 1 : 0;
   return a;
 }
 
@@ -1031,10 +1222,10 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   sa.G = G;
   sa.budget = params->budget;
   sa.mode = 0;
-  sa.ntiles = ntiles_of(cache);
+  sa.ntiles = ntiles_of(cache, G);
   sa.capp = round32(cache->cap);
   sa.bcap = bcap_of(cache, params->budget);
-  if (SCLayout(sa.capp, sa.bcap, 0).total > kMaxSmem) return TRI_ERR_UNSUPPORTED;
+  if (SCLayout(sa.capp, sa.bcap).total > kMaxSmem) return TRI_ERR_UNSUPPORTED;
   TileArgs ta = tile_args(cache, stats, params);
   ta.skip_small = 1;
   ta.raw = reinterpret_cast<float *>(static_cast<char *>(ws) + w.raw_off);

@@ -19,8 +19,12 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;   // CTA size of the long-un
 constexpr int kStageBytes = 16384;              // one pipeline stage (K tile or K+V chunk)
 constexpr int kStages = 4;                      // stages of the score ring
 constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kMaxCompactStages = 16;           // stages of the compaction ring, at most
-constexpr int kTileKeys = 2048;                 // keys per CTA in the split (long-unit) path
+constexpr int kCompactStages = 12;              // stages of the long-unit compaction ring, at least
+constexpr int kMaxCompactStages = 13;           // and at most (bounded by shared memory)
+// Keys per CTA in the split (long-unit) path: the tile's G rows of fp32 scores
+// sit in shared memory next to the 64 KB ring; 1024 keys for G = 8 keep two CTAs
+// per SM.
+__host__ __device__ constexpr int tile_keys_for(int G) { return G >= 8 ? 1024 : 2048; }
 constexpr int kSelThreads = 512;                // CTA size of the select/compact kernel
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // bounded device waits: 2 s
 
@@ -28,6 +32,13 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // bounded device w
 __device__ int g_tri_status = 0;
 
 __device__ __forceinline__ void set_status(int code) { atomicCAS(&g_tri_status, 0, code); }
+
+// True once some wait has given up (TRI_ERR_TIMEOUT recorded and not yet
+// cleared): kernels that wait on copies then leave at once instead of waiting
+// out their own limits one CTA after another.
+__device__ __forceinline__ bool timed_out() {
+  return *reinterpret_cast<volatile int *>(&g_tri_status) == TRI_ERR_TIMEOUT;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -99,6 +110,15 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
       "%4, %5}], [%6];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Tiled 2-D tensor load (TMA) of the box at (c0, c1) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
 

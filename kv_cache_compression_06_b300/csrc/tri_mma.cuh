@@ -1,0 +1,189 @@
+// Key scoring on the tensor cores (bf16 caches, rotate-half bands).
+//
+// The two-part score of a key is a dot product of a per-key feature vector
+// with a per-head weight vector (trig-series paragraph and two-part score
+// paragraph of the method's write-up):
+//   s_{h,i} = sum_f Re A_{h,f} * Re k~_{i,f} + Im A_{h,f} * Im k~_{i,f} + W_{h,f} * |k~_{i,f}|
+// i.e. S = X Y with X_i = (Re k~_i, Im k~_i, |k~_i|) (3F features) and
+// Y = (Re A; Im A; W) (3F x G).  Per 16 keys it runs as m16n8k16 bf16 MMAs with
+// fp32 accumulation:
+//   - Re/Im k~ are the cache's own bf16 values (exact operands);
+//   - every weight is split into hi = bf16(w) and lo = bf16(w - hi), and the
+//     MMA sees both (G <= 4: N = 8 columns = [hi of the G heads | lo of the G
+//     heads], summed after; G = 8: two MMAs);
+//   - |k~| is computed in fp32 from the A fragments themselves (the Re and Im
+//     fragments of a band block hold the same (key, band) positions) and split
+//     into hi + lo as well; the lo x lo product is dropped.
+// The split keeps every product to about 2^-16 relative; accumulation is fp32.
+//
+// K arrives in shared memory through 128B-swizzled tensor copies: a stage is
+// [half][TR rows][128 B] (d = 128: half 0 = Re (elements 0..63), half 1 = Im;
+// d = 64: one half holding both), the 16-byte chunk c of row r stored at chunk
+// c ^ (r & 7), which makes the ldmatrix row reads conflict-free.
+#pragma once
+
+#include "tri_path.cuh"
+
+namespace tri {
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                            uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D += A * B for one m16n8k16 tile (A 16x16 row-major bf16, B 16x8 bf16, fp32 D).
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two fp32 -> one bf16x2 register (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Splits two fp32 values into bf16x2 hi and lo parts (hi + lo ~ v to 2^-16).
+__device__ __forceinline__ void split_bf16x2(float v0, float v1, uint32_t &hi, uint32_t &lo) {
+  hi = pack_bf16x2(v0, v1);
+  lo = pack_bf16x2(v0 - bf16lo(hi), v1 - bf16hi(hi));
+}
+
+// B fragments (weights) of one warp, for D / 16 trig k-steps (Re then Im
+// blocks of 16 bands) and F / 16 magnitude k-steps.
+//   G <= 4: bt[ks] = [hi | lo] columns; bm[ks] = [hi | lo]; bm2[ks] = [hi | 0]
+//   G == 8: bt/bm = hi, bt2/bm2 = lo
+template <int D, int G>
+struct MmaWeights {
+  static constexpr int KT = D / 16, KM = D / 32;
+  uint32_t bt[KT][2], bm[KM][2], bm2[KM][2];
+  uint32_t bt2[G == 8 ? KT : 1][2];
+};
+
+// Builds this lane's B fragments from wts [G][3][F] (Re A, Im A, W).  Lane l
+// holds column n = l / 4 and rows k = 2 (l % 4) + {0, 1, 8, 9} of each k-step.
+template <int D, int G>
+__device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, const float *wts) {
+  constexpr int F = D / 2;
+  const int lane = threadIdx.x & 31, n = lane >> 2, k0 = 2 * (lane & 3);
+  const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
+  // column n of the split weights: head h, part (0 = hi, 1 = lo), or none
+  const int h = G == 8 ? n : (n & 3);
+  const bool live = G == 8 || h < G;
+  const int part = G == 8 ? 0 : (n >> 2);
+#pragma unroll
+  for (int ks = 0; ks < MmaWeights<D, G>::KT; ++ks) {
+    // features 16 ks + k: Re A for bands < F, Im A after
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int f = 16 * ks + kk[e];
+      v[e] = live ? (f < F ? wts[(h * 3 + 0) * F + f] : wts[(h * 3 + 1) * F + f - F]) : 0.f;
+    }
+    uint32_t h01, l01, h23, l23;
+    split_bf16x2(v[0], v[1], h01, l01);
+    split_bf16x2(v[2], v[3], h23, l23);
+    w.bt[ks][0] = part ? l01 : h01;
+    w.bt[ks][1] = part ? l23 : h23;
+    if constexpr (G == 8) {
+      w.bt2[ks][0] = l01;
+      w.bt2[ks][1] = l23;
+    }
+  }
+#pragma unroll
+  for (int ks = 0; ks < MmaWeights<D, G>::KM; ++ks) {
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = live ? wts[(h * 3 + 2) * F + 16 * ks + kk[e]] : 0.f;
+    uint32_t h01, l01, h23, l23;
+    split_bf16x2(v[0], v[1], h01, l01);
+    split_bf16x2(v[2], v[3], h23, l23);
+    if constexpr (G == 8) {
+      w.bm[ks][0] = h01;
+      w.bm[ks][1] = h23;
+      w.bm2[ks][0] = l01;
+      w.bm2[ks][1] = l23;
+    } else {
+      w.bm[ks][0] = part ? l01 : h01;
+      w.bm[ks][1] = part ? l23 : h23;
+      w.bm2[ks][0] = part ? 0u : h01;
+      w.bm2[ks][1] = part ? 0u : h23;
+    }
+  }
+}
+
+// Shared-memory byte address of element column `col` (a multiple of 8) of row
+// `row` in a swizzled stage of TR rows.
+template <int TR>
+__device__ __forceinline__ uint32_t sw_addr(uint32_t stage, int row, int col) {
+  return stage + (uint32_t)((col >> 6) * (TR * 128) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
+}
+
+// Scores the 16 keys at stage rows [r0, r0 + 16) (row0 + r0 + i is the key's
+// index in the caller's score rows); rows at or past nrows are not stored.
+template <int D, int G, int TR>
+__device__ __forceinline__ void score_tile_mma(uint32_t stage, int r0, int nrows, int row0, float *scores,
+                                               int sstride, const MmaWeights<D, G> &w) {
+  constexpr int F = D / 2;
+  const int lane = threadIdx.x & 31;
+  const int lrow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row of this lane
+  const int lcol = (lane >> 4) * 8;                           // and column offset
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < F / 16; ++ks) {
+    uint32_t re[4], im[4];
+    ldmatrix_x4(re[0], re[1], re[2], re[3], sw_addr<TR>(stage, lrow, 16 * ks + lcol));
+    ldmatrix_x4(im[0], im[1], im[2], im[3], sw_addr<TR>(stage, lrow, F + 16 * ks + lcol));
+    mma_bf16(acc, re, w.bt[ks][0], w.bt[ks][1]);
+    mma_bf16(acc, im, w.bt[F / 16 + ks][0], w.bt[F / 16 + ks][1]);
+    if constexpr (G == 8) {
+      mma_bf16(acc, re, w.bt2[ks][0], w.bt2[ks][1]);
+      mma_bf16(acc, im, w.bt2[F / 16 + ks][0], w.bt2[F / 16 + ks][1]);
+    }
+    // |k~| at the same fragment positions, split into hi + lo
+    uint32_t mh[4], ml[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float a, b;
+      upk(ffma2(pk(bf16lo(im[e]), bf16hi(im[e])), pk(bf16lo(im[e]), bf16hi(im[e])),
+                fmul2(pk(bf16lo(re[e]), bf16hi(re[e])), pk(bf16lo(re[e]), bf16hi(re[e])))),
+          a, b);
+      split_bf16x2(sqrt_approx(a), sqrt_approx(b), mh[e], ml[e]);
+    }
+    mma_bf16(acc, mh, w.bm[ks][0], w.bm[ks][1]);
+    if constexpr (G == 8) {
+      mma_bf16(acc, mh, w.bm2[ks][0], w.bm2[ks][1]);   // hi x lo
+      mma_bf16(acc, ml, w.bm[ks][0], w.bm[ks][1]);     // lo x hi
+    } else {
+      mma_bf16(acc, ml, w.bm2[ks][0], w.bm2[ks][1]);   // lo x hi (lo columns get 0)
+    }
+  }
+  // D fragment: acc[0..1] row r, columns n, n + 1; acc[2..3] row r + 8.
+  const int r = lane >> 2, n = 2 * (lane & 3);
+  if constexpr (G == 8) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int row = r0 + r + (e >> 1) * 8;
+      if (row < nrows) scores[(n + (e & 1)) * sstride + row0 + row] = acc[e];
+    }
+  } else {
+    float o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = acc[e] + __shfl_xor_sync(0xffffffffu, acc[e], 2);   // hi + lo
+    if (n < 4) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = r0 + r + (e >> 1) * 8, h = n + (e & 1);
+        if (h < G && row < nrows) scores[h * sstride + row0 + row] = o[e];
+      }
+    }
+  }
+}
+
+}  // namespace tri

@@ -438,26 +438,35 @@ __device__ bool stream_and_score(const CacheView &c, const CUtensorMap *tmk, int
 
 // ---------------------------------------------------------------- GQA moments (a3)
 // Population mean and 1/std per head over scores[h * sstride + i], i < n (two
-// passes over shared memory).  inv = 0 when std = 0 (z = 0).
+// passes over shared memory).  inv = 0 when std = 0 (z = 0).  The sums are
+// taken of the scores minus the head's first score (z does not depend on a
+// shift): a head whose scores are all equal then has exactly zero deviation,
+// and cancellation stays small when the mean is large against the spread.
 template <int G>
 __device__ __forceinline__ void head_moments(const float *scores, int sstride, int n, float *red,
                                              float (&mu)[G], float (&inv)[G]) {
-  float v[G];
+  float v[G], sh[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) v[h] = 0.f;
+  for (int h = 0; h < G; ++h) {
+    v[h] = 0.f;
+    sh[h] = scores[h * sstride];
+  }
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) v[h] += scores[h * sstride + i];
+    for (int h = 0; h < G; ++h) v[h] += scores[h * sstride + i] - sh[h];
   }
   block_sum<G>(v, red);
+  float md[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) mu[h] = v[h] / (float)n;
-#pragma unroll
-  for (int h = 0; h < G; ++h) v[h] = 0.f;
+  for (int h = 0; h < G; ++h) {
+    md[h] = v[h] / (float)n;
+    mu[h] = sh[h] + md[h];
+    v[h] = 0.f;
+  }
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float dlt = scores[h * sstride + i] - mu[h];
+      const float dlt = (scores[h * sstride + i] - sh[h]) - md[h];
       v[h] = fmaf(dlt, dlt, v[h]);
     }
   }

@@ -150,11 +150,16 @@ def key_scores(center, R, m, k_post, pos, t, offsets, theta, pairing="half"):
 
 def gqa_aggregate(s: np.ndarray) -> np.ndarray:
     """z-score each query head's scores over the unit's keys (population sigma,
-    sigma = 0 -> z = 0), then take the max over the heads  [W3-PRUNE]."""
+    sigma = 0 -> z = 0), then take the max over the heads  [W3-PRUNE].
+
+    The moments are taken of the scores minus the head's first score (z is
+    unchanged by a shift), so a head whose scores are all equal has exactly zero
+    deviation and gets z = 0 rather than a rounding artefact of the mean."""
     s = np.asarray(s, dtype=np.float64)
-    mu = s.mean(axis=1, keepdims=True)
-    sd = np.sqrt(((s - mu) ** 2).mean(axis=1, keepdims=True))
-    z = np.where(sd > 0, (s - mu) / np.where(sd > 0, sd, 1.0), 0.0)
+    d = s - s[:, :1]
+    mu = d.mean(axis=1, keepdims=True)
+    sd = np.sqrt(((d - mu) ** 2).mean(axis=1, keepdims=True))
+    z = np.where(sd > 0, (d - mu) / np.where(sd > 0, sd, 1.0), 0.0)
     return np.fmax.reduce(z, axis=0)
 
 

@@ -1,0 +1,79 @@
+"""GPU edge cases against the fp64 oracle, on small seeded workloads that reach
+every kernel variant: the fused short-unit kernel and the split long-unit path
+(tensor-core and CUDA-core scoring), dense and paged caches (16- and 32-token
+blocks), G = 1, 2, 4, 8, head dim 64 and 128, bf16 and fp32, both band
+pairings, ragged lengths with units at N < B, N = B and N = B + 1 in one call,
+t != N, and a unit whose keys are all equal (every score ties).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from synth import Workload, generate
+from tests import _gpu_check as C
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+GEO16 = tuple(2 ** i for i in range(17))
+GEO10 = tuple(2 ** i for i in range(11))
+
+
+def W(name, **kw):
+    base = dict(L=1, S=3, Hq=8, Hkv=2, d=128, theta=1e6, dtype="bf16", budget=512, offsets=GEO16)
+    base.update(kw)
+    return Workload(name=name, **base)
+
+
+CASES = [
+    # fused short-unit kernel
+    W("edge_fused_g1_bf16", Hq=2, n_range=(300, 900)),
+    W("edge_fused_g2_inter_d64", Hq=4, d=64, pairing="interleaved", n_range=(500, 1500)),
+    W("edge_fused_g4_f32", Hq=8, dtype="f32", n_range=(600, 1800), budget=700),
+    W("edge_fused_g8_bf16", Hq=16, n_range=(1000, 3000), budget=1024),
+    W("edge_fused_paged16_g4", Hq=8, n_range=(700, 2500), paged=True),
+    W("edge_fused_paged32_g2_d64", Hq=4, d=64, n_range=(700, 2500), paged=True, block=32),
+    # split long-unit path (scores larger than one CTA's shared memory)
+    W("edge_long_mma_g4", Hq=8, n_range=(9000, 13000), budget=1024),
+    W("edge_long_mma_g8_d64", Hq=16, d=64, n_range=(15000, 20000), budget=2048),
+    W("edge_long_mma_g1", Hq=2, n_range=(40000, 60000), budget=4096, S=2),
+    W("edge_long_mma_g2_paged", Hq=4, n_range=(26000, 30000), budget=1024, paged=True, S=2),
+    W("edge_long_mma_g8_paged32", Hq=16, n_range=(12000, 16000), budget=1024, paged=True, block=32),
+    W("edge_long_cuda_f32_g2", Hq=4, d=64, dtype="f32", n_range=(30000, 40000), budget=2048, S=2),
+    W("edge_long_cuda_inter_g4", Hq=8, pairing="interleaved", n_range=(11000, 14000), budget=1024),
+]
+
+
+@pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
+def test_edge_every_unit(w):
+    data = generate(w, device=DEV)
+    units = [(0, s, g) for s in range(w.S) for g in range(w.Hkv)]
+    C.run_and_check(w, data, units, DEV)
+
+
+def test_budget_boundaries_and_t_offset():
+    """One call with N = B - 1, B, B + 1 and a long unit; t = N + 37."""
+    w = W("edge_bounds", Hq=8, S=4, budget=1000, n_keys=1200)
+    data = generate(w, device=DEV)
+    lens = [999, 1000, 1001, 1200]
+    data["seq_len"] = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    data["t"] = data["seq_len"] + 37
+    w2 = dataclasses.replace(w, n_keys=None, n_range=(999, 1200))
+    object.__setattr__(w2, "seq_lengths", lambda: lens)
+    units = [(0, s, g) for s in range(4) for g in range(w.Hkv)]
+    C.run_and_check(w2, data, units, DEV)
+
+
+@pytest.mark.parametrize("n_keys", [800, 20000])
+def test_all_zero_keys_tie_everywhere(n_keys):
+    """A unit whose keys are all zero (a cleared or padded region): every score
+    is exactly 0 on both sides, the z-score of each head is 0/0 := 0, all keys
+    tie, the lowest B slots are kept and nothing moves (fused path at N = 800,
+    split path at N = 20000)."""
+    w = W(f"edge_ties_{n_keys}", Hq=4, S=1, Hkv=2, budget=300, n_keys=n_keys)
+    data = generate(w, device=DEV)
+    data["k"][0, 0, 1].zero_()          # KV head 1
+    # the zero unit must keep exactly slots 0..B-1: no difference, even in the tie band
+    assert C.run_and_check(w, data, [(0, 0, 1)], DEV) == 0
+    C.run_and_check(w, generate(w, device=DEV), [(0, 0, 0)], DEV)

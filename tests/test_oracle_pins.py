@@ -226,6 +226,16 @@ def test_zscore_sigma_zero_gives_zero():
     np.testing.assert_allclose(a, np.maximum(0.0, z1))
 
 
+def test_zscore_of_a_constant_head_is_exactly_zero():
+    """A value whose running sum is inexact (0.1 * 800 is not 80 in binary):
+    the z-score of a constant head is 0/0 and is defined as 0, exactly."""
+    s = np.full((2, 800), 0.1)
+    s[1] *= -7.3
+    assert np.all(O.gqa_aggregate(s) == 0.0)
+    naive_mu = s.mean(axis=1, keepdims=True)
+    assert np.any(s != naive_mu)   # the unshifted mean is off by rounding here
+
+
 # ---------------------------------------------------------------- top-B
 @pytest.mark.parametrize("seed", range(12))
 def test_topb_matches_exhaustive_search(seed):
