@@ -173,7 +173,7 @@ def _traffic_record(kernel_src_hash, workload, layers):
 def kernel_src_hash():
     import hashlib
     h = hashlib.sha1()
-    for f in ("tri.cu", "tri_path.cuh", "tri_device.cuh"):
+    for f in ("tri.cu", "tri_path.cuh", "tri_device.cuh", "tri_mma.cuh"):
         with open(os.path.join(ROOT, "kv_cache_compression_06_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -220,7 +220,7 @@ def run_b300(args, w):
     del data["q_pre"]
     params = tk.Params(w.theta, data["t"], w.offsets, w.budget, pairing=w.pairing)
     ws = tk.workspace(cache, stats, params)
-    launches = 1 if ws is None else 2
+    launches = 1 if ws is None else 3   # fused kernel, or phases + score tiles + select/compact
     k0, v0 = cache.k.clone(), cache.v.clone()
     L = cache.L
     idx = torch.empty((L, w.S, w.Hkv, w.budget), dtype=torch.int32, device=dev)
@@ -317,7 +317,8 @@ def run_b300(args, w):
         return
     peak, peak_kind = _peaks()
     achieved = alg_bytes / t_step / 1e9
-    kname = f"fused_kernel<{w.d},{w.G},{w.dtype}>" if launches == 1 else "score_tiles_kernel+select_compact_kernel"
+    kname = (f"fused_kernel<{w.d},{w.G},{w.dtype}>" if launches == 1
+             else "phase_kernel+score_tiles_mma_kernel+select_compact_kernel")
     line = {
         "metric": METRIC, "value": world * n_keys / t_step, "unit": "keys/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,

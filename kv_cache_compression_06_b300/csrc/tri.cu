@@ -217,6 +217,15 @@ __device__ __forceinline__ Pipe make_pipe(char *smem, int bars) {
   return p;
 }
 
+// ---------------------------------------------------------------- long units: step phases
+// E[s][f] = e^{i*omega_f*t_s} * Phi_f for every sequence and band, once per call
+// (the tile CTAs of a unit all need it; computing it per tile cost ~20
+// instructions per key at G = 8).
+__global__ void __launch_bounds__(64) phase_kernel(const int *t, int F, float2 *phase, const StepConst sc) {
+  const int s = blockIdx.x;
+  for (int f = threadIdx.x; f < F; f += blockDim.x) phase[(long long)s * F + f] = step_phase(sc, f, t[s]);
+}
+
 // ---------------------------------------------------------------- long units: tiles
 struct TileArgs {
   TmaMaps maps;      // k4 (CUDA-core variant)
@@ -226,7 +235,8 @@ struct TileArgs {
   int Hq;
   const int *t;
   int budget, skip_small, inter, ntiles, mma_ok;
-  long long raw_stride;   // floats between the raw rows of two heads (cap, or capp in the workspace)
+  long long raw_stride;
+  const float2 *phase;   // [S][F] step phases (phase_kernel)   // floats between the raw rows of two heads (cap, or capp in the workspace)
   float *raw;      // [(u*G + h)*raw_stride + i]
   float2 *part;    // [(u*ntiles + tile)*G + h] = (mean, M2) of the tile
   StepConst sc;
@@ -235,13 +245,16 @@ struct TileArgs {
 // per-head score stride of a tile (= 4 mod 32: no bank conflicts)
 __host__ __device__ constexpr int tile_stride_for(int G) { return tile_keys_for(G) + 4; }
 
+// sbt caches the tile's block ids (paged caches with block maps; blocks hold at
+// least 2 rows there, so a tile spans at most tile_keys / 2 + 1 blocks).
 struct TileLayout {
-  int bars, wts, red, scores, total;
+  int bars, wts, red, sbt, scores, total;
   __host__ __device__ TileLayout(int G, int F) {
     int o = kRingBytes;
     bars = o;   o += 128;
     wts = o;    o += align_up(G * 3 * F * 4, 128);
     red = o;    o += 512;
+    sbt = o;    o += align_up((tile_keys_for(G) / 2 + 1) * 4, 128);
     scores = o; o += G * tile_stride_for(G) * 4;
     total = o;
   }
@@ -308,16 +321,17 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   const int i0 = tile * TK;
   if (i0 >= N) return;
   const int n = min(TK, N - i0);
-  if (!c.blocks_ok(s, n, i0)) {
+  int *sbt = reinterpret_cast<int *>(smem + lay.sbt);
+  if (!c.blocks_ok(s, n, i0, c.tm_ok ? sbt : nullptr)) {
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
   if (tid == 0) pipe_init(pipe);
-  build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc);
+  build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc, a.phase + (long long)s * F);
   __syncthreads();
   LaneWeights<G> lw;
   load_lane_weights<G, F>(lw, wts, (tid & 31) % RowGeom<D, BF16>::LPR);
-  if (!stream_and_score<D, G, BF16>(c, &a.maps.k4, l, s, g, i0, n, pipe, scores, TS, lw,
+  if (!stream_and_score<D, G, BF16>(c, &a.maps.k4, sbt, l, s, g, i0, n, pipe, scores, TS, lw,
                                     a.inter != 0))
     return;
   for (int i = tid; i < n; i += nt) {
@@ -339,9 +353,9 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
 // loaded too and never scored, rows past the tensor read as zero.  Paged: one
 // copy per block and half.  Called by all lanes of the producer warp.
 template <int D>
-__device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUtensorMap *map, int l, int s, int g,
-                                                 long long urow0, int row0, int nrows, char *dst, uint64_t *full,
-                                                 int lane) {
+__device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUtensorMap *map, const int *sbt,
+                                                 int b0, int l, int s, int g, long long urow0, int row0,
+                                                 int nrows, char *dst, uint64_t *full, int lane) {
   constexpr int TR = kStageBytes / (2 * D), NH = D / 64;   // rows per stage, halves per row
   if (!c.paged()) {
     if (lane == 0) {
@@ -355,7 +369,7 @@ __device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUten
   if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nblk * blk * 128 * NH));
   __syncwarp();
   if (lane < nblk) {
-    const int b = c.bt[(long long)s * c.max_blocks + row0 / blk + lane];
+    const int b = sbt[row0 / blk + lane - b0];
     const int z = (int)((long long)l * c.nblocks + b);
 #pragma unroll
     for (int hh = 0; hh < NH; ++hh) tma_load_4d(dst + hh * TR * 128 + lane * blk * 128, map, 64 * hh, g, 0, z, full);
@@ -393,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
   const int i0 = tile * TK;
   if (i0 >= N) return;
   const int n = min(TK, N - i0);
-  if (!c.blocks_ok(s, n, i0)) {
+  int *sbt = reinterpret_cast<int *>(smem + lay.sbt);
+  if (!c.blocks_ok(s, n, i0, c.tm_ok ? sbt : nullptr)) {
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
@@ -406,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
     *pipe.issued = 0;
     fence_mbar_init();
   }
-  build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc);
+  build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc, a.phase + (long long)s * F);
   __syncthreads();
   const int ntiles = (n + TR - 1) / TR;
   const long long urow0 = (long long)u * c.cap;   // dense: row of slot 0 in the 2-D view
@@ -418,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
         *pipe.fail = 1;
         break;
       }
-      produce_stage_sw<D>(c, &a.ks, l, s, g, urow0, i0 + t * TR, min(TR, n - t * TR),
-                          pipe.ring + st * kStageBytes, &pipe.full[st], lane);
+      produce_stage_sw<D>(c, &a.ks, sbt, c.paged() ? i0 / c.block : 0, l, s, g, urow0, i0 + t * TR,
+                          min(TR, n - t * TR), pipe.ring + st * kStageBytes, &pipe.full[st], lane);
     }
     if (lane == 0) *pipe.issued = t;
   } else {
@@ -569,7 +584,7 @@ struct SCLayout {
                             kStageBytes);
     o += kb;
     nstages = min(kMaxCompactStages, kb / kStageBytes);
-    bars = o; o += kMaxCompactStages * 8;
+    bars = o; o += 2 * kMaxCompactStages * 8;
     hist = o; o += 1024;
     sm = o;   o += kSelInts * 4;
     mom = o;  o += 128;
@@ -581,15 +596,15 @@ struct SCLayout {
 
 
 // a3 for one long unit from its raw scores: the G rows raw[h][0..N) (stride
-// capp floats, 16-byte aligned) are read with 16-byte loads, U*G of them in
-// flight per thread; every thread turns its keys into z = max_h (s_h - mean_h) /
-// std_h, writes the order-preserving keys (4 per store) and adds them to the
-// top-byte histogram.  Key slots in [N, round4(N)) receive don't-care values.
+// capp floats, 16-byte aligned) are read with 16-byte loads, U*G of them per
+// thread and batch, the next batch's loads issued before the current batch is
+// used; every thread turns its keys into z = max_h (s_h - mean_h) / std_h and
+// writes the order-preserving keys (4 per store).  Key slots in
+// [N, round4(N)) receive don't-care values.
 template <int G>
-__device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *mom, uint32_t *keys,
-                              uint32_t *hist) {
+__device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *mom, uint32_t *keys) {
   constexpr int U = G >= 8 ? 1 : 8 / G;
-  const int tid = threadIdx.x, lane = tid & 31, nt = blockDim.x;
+  const int tid = threadIdx.x, nt = blockDim.x;
   float mu[G], iv[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -597,42 +612,43 @@ __device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *
     iv[h] = mom[8 + h];
   }
   const int n4 = (N + 3) / 4;
-  for (int base = tid & ~31; base < n4; base += nt * U) {
-    float4 v[U][G];
+  const float4 *rows = reinterpret_cast<const float4 *>(raw_u);
+  const int hs = capp / 4;   // float4 stride between heads
+  float4 cur[U][G], nxt[U][G];
+  auto load = [&](float4 (&v)[U][G], int base) {
 #pragma unroll
     for (int k = 0; k < U; ++k) {
-      const int q = base + k * nt + lane;
+      const int q = base + k * nt;
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        v[k][h] = q < n4 ? __ldg(reinterpret_cast<const float4 *>(raw_u + (long long)h * capp) + q)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int h = 0; h < G; ++h) v[k][h] = q < n4 ? __ldg(rows + (long long)h * hs + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  };
+  load(cur, tid);
+  for (int base = tid; base < n4; base += nt * U) {
+    load(nxt, base + nt * U);
 #pragma unroll
     for (int k = 0; k < U; ++k) {
-      const int q = base + k * nt + lane;
+      const int q = base + k * nt;
       float z[4];
-      z[0] = (v[k][0].x - mu[0]) * iv[0];
-      z[1] = (v[k][0].y - mu[0]) * iv[0];
-      z[2] = (v[k][0].z - mu[0]) * iv[0];
-      z[3] = (v[k][0].w - mu[0]) * iv[0];
+      z[0] = (cur[k][0].x - mu[0]) * iv[0];
+      z[1] = (cur[k][0].y - mu[0]) * iv[0];
+      z[2] = (cur[k][0].z - mu[0]) * iv[0];
+      z[3] = (cur[k][0].w - mu[0]) * iv[0];
 #pragma unroll
       for (int h = 1; h < G; ++h) {
-        z[0] = fmaxf(z[0], (v[k][h].x - mu[h]) * iv[h]);
-        z[1] = fmaxf(z[1], (v[k][h].y - mu[h]) * iv[h]);
-        z[2] = fmaxf(z[2], (v[k][h].z - mu[h]) * iv[h]);
-        z[3] = fmaxf(z[3], (v[k][h].w - mu[h]) * iv[h]);
+        z[0] = fmaxf(z[0], (cur[k][h].x - mu[h]) * iv[h]);
+        z[1] = fmaxf(z[1], (cur[k][h].y - mu[h]) * iv[h]);
+        z[2] = fmaxf(z[2], (cur[k][h].z - mu[h]) * iv[h]);
+        z[3] = fmaxf(z[3], (cur[k][h].w - mu[h]) * iv[h]);
       }
-      uint4 kk;
-      kk.x = score_key(z[0]);
-      kk.y = score_key(z[1]);
-      kk.z = score_key(z[2]);
-      kk.w = score_key(z[3]);
-      if (q < n4) reinterpret_cast<uint4 *>(keys)[q] = kk;
-      hist_add_top(hist, kk.x, 4 * q + 0 < N);
-      hist_add_top(hist, kk.y, 4 * q + 1 < N);
-      hist_add_top(hist, kk.z, 4 * q + 2 < N);
-      hist_add_top(hist, kk.w, 4 * q + 3 < N);
+      if (q < n4)
+        reinterpret_cast<uint4 *>(keys)[q] = make_uint4(score_key(z[0]), score_key(z[1]), score_key(z[2]),
+                                                        score_key(z[3]));
     }
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+#pragma unroll
+      for (int h = 0; h < G; ++h) cur[k][h] = nxt[k][h];
   }
 }
 
@@ -668,7 +684,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
     return;
   }
   if (tid == 0) {
-    for (int st = 0; st < lay.nstages; ++st) mbar_init(&cbars[st], 1);
+    for (int st = 0; st < lay.nstages; ++st) {
+      mbar_init(&cbars[st], 1);                       // K warp
+      mbar_init(&cbars[kMaxCompactStages + st], 1);   // V warp
+    }
     fence_mbar_init();
   }
   if (a.mode == 2) {
@@ -689,33 +708,27 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
     __syncthreads();
     const int e0 = sm[56];
     __syncthreads();
-    if ((tid >> 5) == 0) compact_unit_tma(c, &a.maps, l, s, g, idxs, e0, B, N, ring, lay.nstages, cbars);
+    if ((tid >> 5) < 2)
+      compact_unit_tma(c, &a.maps, tid >> 5, l, s, g, idxs, e0, B, N, ring, lay.nstages,
+                       cbars + (tid >> 5) * kMaxCompactStages);
     return;
   }
-  for (int b = tid; b < 256; b += nt) hist[b] = 0;
   if (a.mode == 0) {
     merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom);
     __syncthreads();
     const float *raw_u = a.raw + (long long)u * a.G * a.capp;
     switch (a.G) {
-      case 1: zmax_from_raw<1>(raw_u, a.capp, N, mom, keys, hist); break;
-      case 2: zmax_from_raw<2>(raw_u, a.capp, N, mom, keys, hist); break;
-      case 4: zmax_from_raw<4>(raw_u, a.capp, N, mom, keys, hist); break;
-      default: zmax_from_raw<8>(raw_u, a.capp, N, mom, keys, hist); break;
+      case 1: zmax_from_raw<1>(raw_u, a.capp, N, mom, keys); break;
+      case 2: zmax_from_raw<2>(raw_u, a.capp, N, mom, keys); break;
+      case 4: zmax_from_raw<4>(raw_u, a.capp, N, mom, keys); break;
+      default: zmax_from_raw<8>(raw_u, a.capp, N, mom, keys); break;
     }
-    __syncthreads();
   } else {
-    __syncthreads();
-    for (int base = tid & ~31; base < N; base += nt) {
-      const int i = base + lane;
-      const uint32_t key = i < N ? score_key(a.agg[(long long)u * c.cap + i]) : 0u;
-      if (i < N) keys[i] = key;
-      hist_add_top(hist, key, i < N);
-    }
-    __syncthreads();
+    for (int i = tid; i < N; i += nt) keys[i] = score_key(a.agg[(long long)u * c.cap + i]);
   }
+  __syncthreads();
   int ntie;
-  const uint32_t T = radix_select(keys, N, B, hist, sm, &ntie, true);
+  const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
   const int e0 = build_kept(keys, N, B, T, ntie, idxs, sm);
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
@@ -724,7 +737,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
     // stores; TMA writes them next.
     fence_proxy_async_smem();
     __syncthreads();
-    if ((tid >> 5) == 0) compact_unit_tma(c, &a.maps, l, s, g, idxs, e0, B, N, ring, lay.nstages, cbars);
+    if ((tid >> 5) < 2)
+      compact_unit_tma(c, &a.maps, tid >> 5, l, s, g, idxs, e0, B, N, ring, lay.nstages,
+                       cbars + (tid >> 5) * kMaxCompactStages);
   }
 }
 
@@ -921,21 +936,29 @@ static bool fused_fits(const tri_cache *c, int G) {
 }
 
 struct SplitWs {
-  size_t raw_off, part_off, total;
+  size_t raw_off, part_off, phase_off, total;
 };
 static SplitWs split_ws(const tri_cache *c, int G) {
   SplitWs w;
   // raw rows padded to round32(cap) floats: 16-byte aligned for bulk copies
   const size_t raw = (size_t)units_of(c) * G * (size_t)round32(c->cap) * sizeof(float);
   const size_t part = (size_t)units_of(c) * ntiles_of(c, G) * G * sizeof(float2);
+  const size_t phase = (size_t)c->S * (c->d / 2) * sizeof(float2);
   w.raw_off = 0;
   w.part_off = (raw + 255) / 256 * 256;
-  w.total = w.part_off + (part + 255) / 256 * 256;
+  w.phase_off = w.part_off + (part + 255) / 256 * 256;
+  w.total = w.phase_off + (phase + 255) / 256 * 256;
   return w;
 }
 
 static tri_status launch_result() {
   return cudaGetLastError() == cudaSuccess ? TRI_OK : TRI_ERR_CUDA;
+}
+
+// Fills the workspace's step phases (before the tile kernels).
+static tri_status run_phases(const tri_cache *c, const TileArgs &ta, cudaStream_t st) {
+  phase_kernel<<<(unsigned)c->S, 64, 0, st>>>(ta.t, c->d / 2, const_cast<float2 *>(ta.phase), ta.sc);
+  return launch_result();
 }
 
 template <typename K>
@@ -1139,6 +1162,8 @@ tri_status tri_score(const tri_cache *cache, const tri_stats *stats, const tri_p
   ta.raw = raw != nullptr ? raw : reinterpret_cast<float *>(static_cast<char *>(ws) + w.raw_off);
   ta.raw_stride = raw != nullptr ? cache->cap : round32(cache->cap);
   ta.part = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.part_off);
+  ta.phase = reinterpret_cast<const float2 *>(static_cast<char *>(ws) + w.phase_off);
+  if ((e = run_phases(cache, ta, stream)) != TRI_OK) return e;
   if ((e = TRI_DISPATCH(run_tiles, cache->d, G, bf16, ta, units, stream)) != TRI_OK) return e;
   ZArgs z;
   z.S = cache->S;
@@ -1231,6 +1256,8 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   ta.raw = reinterpret_cast<float *>(static_cast<char *>(ws) + w.raw_off);
   ta.raw_stride = sa.capp;
   ta.part = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.part_off);
+  ta.phase = reinterpret_cast<const float2 *>(static_cast<char *>(ws) + w.phase_off);
+  if ((e = run_phases(cache, ta, stream)) != TRI_OK) return e;
   if ((e = TRI_DISPATCH(run_tiles, cache->d, G, bf16, ta, units, stream)) != TRI_OK) return e;
   sa.raw = ta.raw;
   sa.part = ta.part;

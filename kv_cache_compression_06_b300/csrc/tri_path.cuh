@@ -58,46 +58,54 @@ struct CacheView {
     return (((long long)l * nblocks + b) * block + (i % block)) * Hkv + g;
   }
   // Checks every block id that rows [row0, row0 + n) of sequence s touch
-  // (CTA-wide; every thread gets the answer).
-  __device__ bool blocks_ok(int s, int n, int row0 = 0) const {
+  // (CTA-wide; every thread gets the answer).  If `keep` is given, the ids are
+  // also stored there (keep[b - row0 / block]) for the copy issue path.
+  __device__ bool blocks_ok(int s, int n, int row0 = 0, int *keep = nullptr) const {
     if (bt == nullptr) return true;
     const int b0 = row0 / block, nb = (row0 + n + block - 1) / block;
     int bad = 0;
     for (int b = b0 + threadIdx.x; b < nb; b += blockDim.x) {
       const int id = bt[(long long)s * max_blocks + b];
       bad |= (id < 0 || id >= nblocks);
+      if (keep != nullptr) keep[b - b0] = id;
     }
     return __syncthreads_or(bad) == 0;
   }
 };
 
 // ---------------------------------------------------------------- weights (a1)
-// wts layout [G][3][F]: Re A, Im A, W for the G query heads of KV head g.
-// A_{h,f} = c_{h,f} * e^{i*omega_f*t} * Phi_f; W_{h,f} = (1 - R_{h,f}) * m_{h,f}.
-// The phase omega_f*t is reduced modulo 2*pi in fp64 (two-term 2*pi split) before
-// an fp32 sincos: omega_0*t reaches ~3e4 rad, far beyond fp32 phase accuracy.
-template <int G, int F>
-__device__ __forceinline__ void build_weights(float *wts, const float *center, const float *R,
-                                              const float *mag, int Hq, int l, int g, int t,
-                                              const StepConst &sc) {
+// Phase factor of band f for a step at position t: e^{i*omega_f*t} * Phi_f.
+// The phase omega_f*t is reduced modulo 2*pi in fp64 (two-term 2*pi split)
+// before an fp32 sincos: omega_0*t reaches ~3e4 rad, far beyond fp32 phase
+// accuracy.
+__device__ __forceinline__ float2 step_phase(const StepConst &sc, int f, int t) {
   constexpr double kTwoPiHi = 6.283185307179586232;
   constexpr double kTwoPiLo = 2.449293598294706e-16;
   constexpr double kInvTwoPi = 0.15915494309189535;
+  const double ph = sc.omega[f] * (double)t;
+  const double q = rint(ph * kInvTwoPi);
+  double r = fma(-q, kTwoPiHi, ph);
+  r = fma(-q, kTwoPiLo, r);
+  float sn, cs;
+  sincosf((float)r, &sn, &cs);
+  const float2 p = sc.phi[f];
+  return make_float2(cs * p.x - sn * p.y, cs * p.y + sn * p.x);
+}
+
+// wts layout [G][3][F]: Re A, Im A, W for the G query heads of KV head g.
+// A_{h,f} = c_{h,f} * E_f with E_f the step phase of band f (computed here, or
+// taken from `phase` [F] when given); W_{h,f} = (1 - R_{h,f}) * m_{h,f}.
+template <int G, int F>
+__device__ __forceinline__ void build_weights(float *wts, const float *center, const float *R,
+                                              const float *mag, int Hq, int l, int g, int t,
+                                              const StepConst &sc, const float2 *phase = nullptr) {
   for (int x = threadIdx.x; x < G * F; x += blockDim.x) {
     const int h = x / F, f = x - h * F;
     const long long o = ((long long)l * Hq + (long long)g * G + h) * F + f;
-    const double ph = sc.omega[f] * (double)t;
-    const double q = rint(ph * kInvTwoPi);
-    double r = fma(-q, kTwoPiHi, ph);
-    r = fma(-q, kTwoPiLo, r);
-    float sn, cs;
-    sincosf((float)r, &sn, &cs);
-    const float2 p = sc.phi[f];
-    const float er = cs * p.x - sn * p.y;
-    const float ei = cs * p.y + sn * p.x;
+    const float2 e = phase != nullptr ? phase[f] : step_phase(sc, f, t);
     const float cr = center[2 * o], ci = center[2 * o + 1];
-    wts[(h * 3 + 0) * F + f] = cr * er - ci * ei;
-    wts[(h * 3 + 1) * F + f] = cr * ei + ci * er;
+    wts[(h * 3 + 0) * F + f] = cr * e.x - ci * e.y;
+    wts[(h * 3 + 1) * F + f] = cr * e.y + ci * e.x;
     wts[(h * 3 + 2) * F + f] = (1.0f - R[o]) * mag[o];
   }
 }
@@ -356,9 +364,9 @@ __device__ __forceinline__ void pipe_init(const Pipe &p) {
 // of the last block past nrows are loaded too, they exist).  Paged without: one
 // bulk copy per row.  Called by all 32 lanes of the producer warp.
 template <int RB>
-__device__ __forceinline__ void produce_stage(const CacheView &c, const CUtensorMap *tmk, int l, int s,
-                                              int g, int row0, int nrows, char *dst, uint64_t *full,
-                                              int lane) {
+__device__ __forceinline__ void produce_stage(const CacheView &c, const CUtensorMap *tmk, const int *sbt,
+                                              int b0, int l, int s, int g, int row0, int nrows, char *dst,
+                                              uint64_t *full, int lane) {
   if (!c.paged()) {
     if (lane == 0) {
       const uint32_t bytes = (uint32_t)nrows * (uint32_t)RB;
@@ -372,7 +380,7 @@ __device__ __forceinline__ void produce_stage(const CacheView &c, const CUtensor
     if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nblk * blk * RB));
     __syncwarp();
     if (lane < nblk) {
-      const int b = c.bt[(long long)s * c.max_blocks + row0 / blk + lane];
+      const int b = sbt[row0 / blk + lane - b0];
       tma_load_4d(dst + lane * blk * RB, tmk, 0, g, 0, (int)((long long)l * c.nblocks + b), full);
     }
     return;
@@ -393,8 +401,8 @@ __device__ __forceinline__ void produce_stage(const CacheView &c, const CUtensor
 // every thread of the CTA (kThreads); returns false (CTA-uniform, after a
 // barrier) if a wait gave up.  The caller initialised the pipe and synchronised.
 template <int D, int G, bool BF16>
-__device__ bool stream_and_score(const CacheView &c, const CUtensorMap *tmk, int l, int s, int g,
-                                 int row_begin, int n, const Pipe &p, float *scores, int sstride,
+__device__ bool stream_and_score(const CacheView &c, const CUtensorMap *tmk, const int *sbt, int l, int s,
+                                 int g, int row_begin, int n, const Pipe &p, float *scores, int sstride,
                                  const LaneWeights<G> &lw, bool inter) {
   using RG = RowGeom<D, BF16>;
   constexpr int TR = kStageBytes / RG::RB;
@@ -408,8 +416,8 @@ __device__ bool stream_and_score(const CacheView &c, const CUtensorMap *tmk, int
         *p.fail = 1;
         break;
       }
-      produce_stage<RG::RB>(c, tmk, l, s, g, row_begin + t * TR, min(TR, n - t * TR),
-                            p.ring + st * kStageBytes, &p.full[st], lane);
+      produce_stage<RG::RB>(c, tmk, sbt, row_begin / c.block, l, s, g, row_begin + t * TR,
+                            min(TR, n - t * TR), p.ring + st * kStageBytes, &p.full[st], lane);
     }
     if (lane == 0) *p.issued = t;
   } else {
@@ -581,86 +589,6 @@ __device__ __noinline__ int build_kept_chunked(const uint32_t *keys, int n, int 
   const int e0 = sm[36];
   __syncthreads();
   return e0;
-}
-
-// Adds one key per lane (where `valid`) to the histogram of its top byte
-// (the first radix digit).  A score distribution puts most keys into a handful
-// of top bytes, so the lanes of a warp are grouped by digit (ballot per
-// distinct digit) and each group adds its count with one atomic.  Warp-uniform.
-__device__ __forceinline__ void hist_add_top(uint32_t *hist, uint32_t key, bool valid) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t d = key >> 24;
-  unsigned todo = __ballot_sync(0xffffffffu, valid);
-  while (todo != 0u) {
-    const int leader = __ffs(todo) - 1;
-    const uint32_t dl = __shfl_sync(0xffffffffu, d, leader);
-    const unsigned same = __ballot_sync(0xffffffffu, valid && d == dl);
-    if (lane == leader) atomicAdd(&hist[dl], (uint32_t)__popc(same));
-    todo &= ~same;
-  }
-}
-
-// Radix select (8-bit digits, most significant first) of the K-th largest key
-// among keys[0..n).  Returns the threshold key T and, in *ntie, how many keys
-// equal to T are kept (the lowest slots).  If `top_ready`, hist already holds
-// the histogram of the top byte over all n keys (built by hist_add_top while
-// the keys were written) and the first pass only selects.  Needs 256 <=
-// blockDim <= 512, a multiple of 32.  hist: 256 u32.
-__device__ __noinline__ uint32_t radix_select(const uint32_t *keys, int n, int K, uint32_t *hist,
-                                              int *sm, int *ntie, bool top_ready) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
-  uint32_t prefix = 0, mask = 0;
-  int k = K;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    if (shift < 24 || !top_ready) {
-      for (int b = tid; b < 256; b += nt) hist[b] = 0;
-      __syncthreads();
-      if (shift == 24) {
-        for (int base = tid & ~31; base < n; base += nt) {
-          const int i = base + lane;
-          hist_add_top(hist, i < n ? keys[i] : 0u, i < n);
-        }
-      } else {
-        for (int i = tid; i < n; i += nt) {
-          const uint32_t u = keys[i];
-          if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
-        }
-      }
-    }
-    __syncthreads();
-    // Suffix counts S[x] = #{digit >= x}: thread t < 256 scans the reversed
-    // histogram, so its inclusive prefix P_t equals S[255 - t] and P_{t-1}
-    // equals S[256 - t].  The digit x is the one with S[x] >= k > S[x + 1].
-    int P = 0, wsum = 0;
-    if (tid < 256) {
-      P = (int)hist[255 - tid];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, P, o);
-        if (lane >= o) P += y;
-      }
-      if (lane == 31) sm[8 + warp] = P;
-    }
-    __syncthreads();
-    if (tid < 256) {
-      for (int w = 0; w < warp; ++w) wsum += sm[8 + w];
-      P += wsum;
-      int Pprev = __shfl_up_sync(0xffffffffu, P, 1);
-      if (lane == 0) Pprev = wsum;
-      if (P >= k && Pprev < k) {
-        sm[0] = 255 - tid;
-        sm[1] = k - Pprev;
-      }
-    }
-    __syncthreads();
-    const uint32_t dgt = (uint32_t)sm[0];
-    k = sm[1];
-    prefix |= dgt << shift;
-    mask |= 255u << shift;
-    __syncthreads();
-  }
-  *ntie = k;
-  return prefix;
 }
 
 // Writes the kept slots of keys[0..n) (those > T, plus the first ntie equal to
@@ -845,13 +773,21 @@ __device__ __noinline__ bool compact_unit_runs(const CacheView &c, int l, int s,
 // (status recorded; loads already issued are waited for, bounded).
 constexpr int kRunLimit = 8;   // runs per chunk up to which bulk copies beat gather4
 
-__device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps *maps, int l, int s, int g,
-                                              const int *idx, int e0, int B, int N, char *ring,
+// Compacts one tensor (which = 0: K, 1: V) of unit (l, s, g); the calling warp
+// owns it alone (the two tensors are independent arrays, so a K warp and a V
+// warp run side by side, each with its own barriers and bulk groups).  Stage st
+// holds the chunk's K rows at [0, ch) and V rows at [ch, 2ch).
+__device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps *maps, int which, int l, int s,
+                                              int g, const int *idx, int e0, int B, int N, char *ring,
                                               int nstages, uint64_t *cbars) {
   const int lane = threadIdx.x & 31;
   const int rb = c.rb;
   const int ch = min(32, kStageBytes / (2 * rb));   // rows per chunk (a multiple of 4)
   if (B - e0 <= 0) return true;
+  char *base = which ? c.v : c.k;
+  const CUtensorMap *map2 = which ? &maps->v2 : &maps->k2;
+  const CUtensorMap *map4 = which ? &maps->v4 : &maps->k4;
+  const long long toff = (long long)which * ch * rb;   // this tensor's rows within a stage
   const bool paged = c.paged();
   const bool blkst = paged && c.tm_ok && ch % c.block == 0;
   const int jb = blkst ? (e0 / c.block) * c.block : e0;
@@ -859,7 +795,7 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
 
   auto issue_loads = [&](int cidx) {
     const int st = cidx % nstages;
-    char *sk = ring + st * kStageBytes;   // K rows [0, ch), then V rows [ch, 2ch)
+    char *sk = ring + st * kStageBytes + toff;
     const int j0 = jb + cidx * ch;
     const int rows = min(ch, B - j0);
     int src = -1;
@@ -880,24 +816,18 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
     const bool boundary = valid && (paged || lane == 0 || !((vmask >> (lane - 1)) & 1u) || prev + 1 != src);
     const unsigned bmask = __ballot_sync(0xffffffffu, boundary);
     const bool use_runs = !paged && (__popc(bmask) <= kRunLimit || c.g4_ok == 0);
-    int bytes = 0;
     if (use_runs) {
       // one bulk copy per run [lane, next boundary or invalid lane)
+      int end = lane;
       if (boundary) {
         const unsigned stop = (bmask | ~vmask) & (lane == 31 ? 0u : (0xffffffffu << (lane + 1)));
-        const int end = stop ? (__ffs(stop) - 1) : 32;
-        bytes = (end - lane) * rb;
+        end = stop ? (__ffs(stop) - 1) : 32;
       }
-      bytes = 2 * warp_sum_int(bytes);
+      const int bytes = warp_sum_int((end - lane) * rb);
       if (lane == 0) mbar_arrive_expect_tx(&cbars[st], (uint32_t)bytes);
       __syncwarp();
-      if (boundary) {
-        const unsigned stop = (bmask | ~vmask) & (lane == 31 ? 0u : (0xffffffffu << (lane + 1)));
-        const int end = stop ? (__ffs(stop) - 1) : 32;
-        const long long off = r2 * rb;
-        bulk_g2s(sk + (long long)lane * rb, c.k + off, (uint32_t)((end - lane) * rb), &cbars[st]);
-        bulk_g2s(sk + (long long)(ch + lane) * rb, c.v + off, (uint32_t)((end - lane) * rb), &cbars[st]);
-      }
+      if (boundary)
+        bulk_g2s(sk + (long long)lane * rb, base + r2 * rb, (uint32_t)((end - lane) * rb), &cbars[st]);
     } else if (c.g4_ok) {
       // one tile::gather4 per quad of destination rows (lanes past `rows`
       // repeat the quad's first valid row; those smem rows are never stored)
@@ -911,23 +841,15 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
       const int c2 = __shfl_sync(0xffffffffu, rc, q0 + 2);
       const int c3 = __shfl_sync(0xffffffffu, rc, q0 + 3);
       const bool gath = lane == q0 && (vmask & qmask) != 0u;
-      bytes = 2 * warp_sum_int(gath ? 4 * rb : 0);
-      if (lane == 0) mbar_arrive_expect_tx(&cbars[st], (uint32_t)bytes);
+      const unsigned gmask = __ballot_sync(0xffffffffu, gath);
+      if (lane == 0) mbar_arrive_expect_tx(&cbars[st], (uint32_t)(__popc(gmask) * 4 * rb));
       __syncwarp();
-      if (gath) {
-        tma_gather4(sk + (long long)q0 * rb, &maps->k2, 0, c0, c1, c2, c3, &cbars[st]);
-        tma_gather4(sk + (long long)(ch + q0) * rb, &maps->v2, 0, c0, c1, c2, c3, &cbars[st]);
-      }
+      if (gath) tma_gather4(sk + (long long)q0 * rb, map2, 0, c0, c1, c2, c3, &cbars[st]);
     } else {
       // paged without row maps: one bulk copy per row
-      bytes = 2 * warp_sum_int(valid ? rb : 0);
-      if (lane == 0) mbar_arrive_expect_tx(&cbars[st], (uint32_t)bytes);
+      if (lane == 0) mbar_arrive_expect_tx(&cbars[st], (uint32_t)(__popc(vmask) * rb));
       __syncwarp();
-      if (valid) {
-        const long long off = r2 * rb;
-        bulk_g2s(sk + (long long)lane * rb, c.k + off, (uint32_t)rb, &cbars[st]);
-        bulk_g2s(sk + (long long)(ch + lane) * rb, c.v + off, (uint32_t)rb, &cbars[st]);
-      }
+      if (valid) bulk_g2s(sk + (long long)lane * rb, base + r2 * rb, (uint32_t)rb, &cbars[st]);
     }
   };
 
@@ -936,7 +858,7 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
   int cidx = 0;
   for (; cidx < nch; ++cidx) {
     const int st = cidx % nstages;
-    const char *sk = ring + st * kStageBytes;
+    const char *sk = ring + st * kStageBytes + toff;
     const int j0 = jb + cidx * ch;
     const int rows = min(ch, B - j0);
     if (!mbar_wait(&cbars[st], (uint32_t)((cidx / nstages) & 1))) {
@@ -944,25 +866,16 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
       break;
     }
     if (!paged) {
-      if (lane == 0) {
-        const long long off = c.row_off(l, s, g, j0);
-        bulk_s2g(c.k + off, sk, (uint32_t)(rows * rb));
-        bulk_s2g(c.v + off, sk + (long long)ch * rb, (uint32_t)(rows * rb));
-      }
+      if (lane == 0) bulk_s2g(base + c.row_off(l, s, g, j0), sk, (uint32_t)(rows * rb));
     } else if (blkst) {
       const int nb = (rows + c.block - 1) / c.block;
       if (lane < nb) {
         const int b = c.bt[(long long)s * c.max_blocks + j0 / c.block + lane];
-        const int z = (int)((long long)l * c.nblocks + b);
-        tma_store_4d(&maps->k4, 0, g, 0, z, sk + (long long)lane * c.block * rb);
-        tma_store_4d(&maps->v4, 0, g, 0, z, sk + (long long)(ch + lane * c.block) * rb);
+        tma_store_4d(map4, 0, g, 0, (int)((long long)l * c.nblocks + b), sk + (long long)lane * c.block * rb);
       }
     } else if (lane < rows) {
       const long long off = c.row_off(l, s, g, j0 + lane);
-      if (off >= 0) {
-        bulk_s2g(c.k + off, sk + (long long)lane * rb, (uint32_t)rb);
-        bulk_s2g(c.v + off, sk + (long long)(ch + lane) * rb, (uint32_t)rb);
-      }
+      if (off >= 0) bulk_s2g(base + off, sk + (long long)lane * rb, (uint32_t)rb);
     }
     bulk_commit();
     bulk_wait_read<1>();   // the stores of chunk cidx-1 no longer read their stage
