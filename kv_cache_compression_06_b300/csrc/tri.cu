@@ -245,16 +245,13 @@ struct TileArgs {
 // per-head score stride of a tile (= 4 mod 32: no bank conflicts)
 __host__ __device__ constexpr int tile_stride_for(int G) { return tile_keys_for(G) + 4; }
 
-// sbt caches the tile's block ids (paged caches with block maps; blocks hold at
-// least 2 rows there, so a tile spans at most tile_keys / 2 + 1 blocks).
 struct TileLayout {
-  int bars, wts, red, sbt, scores, total;
+  int bars, wts, red, scores, total;
   __host__ __device__ TileLayout(int G, int F) {
     int o = kRingBytes;
     bars = o;   o += 128;
     wts = o;    o += align_up(G * 3 * F * 4, 128);
     red = o;    o += 512;
-    sbt = o;    o += align_up((tile_keys_for(G) / 2 + 1) * 4, 128);
     scores = o; o += G * tile_stride_for(G) * 4;
     total = o;
   }
@@ -321,8 +318,7 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   const int i0 = tile * TK;
   if (i0 >= N) return;
   const int n = min(TK, N - i0);
-  int *sbt = reinterpret_cast<int *>(smem + lay.sbt);
-  if (!c.blocks_ok(s, n, i0, c.tm_ok ? sbt : nullptr)) {
+  if (!c.blocks_ok(s, n, i0)) {
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
@@ -331,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   __syncthreads();
   LaneWeights<G> lw;
   load_lane_weights<G, F>(lw, wts, (tid & 31) % RowGeom<D, BF16>::LPR);
-  if (!stream_and_score<D, G, BF16>(c, &a.maps.k4, sbt, l, s, g, i0, n, pipe, scores, TS, lw,
+  if (!stream_and_score<D, G, BF16>(c, &a.maps.k4, l, s, g, i0, n, pipe, scores, TS, lw,
                                     a.inter != 0))
     return;
   for (int i = tid; i < n; i += nt) {
@@ -353,9 +349,9 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
 // loaded too and never scored, rows past the tensor read as zero.  Paged: one
 // copy per block and half.  Called by all lanes of the producer warp.
 template <int D>
-__device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUtensorMap *map, const int *sbt,
-                                                 int b0, int l, int s, int g, long long urow0, int row0,
-                                                 int nrows, char *dst, uint64_t *full, int lane) {
+__device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUtensorMap *map, int l, int s,
+                                                 int g, long long urow0, int row0, int nrows, char *dst,
+                                                 uint64_t *full, int lane) {
   constexpr int TR = kStageBytes / (2 * D), NH = D / 64;   // rows per stage, halves per row
   if (!c.paged()) {
     if (lane == 0) {
@@ -369,23 +365,65 @@ __device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUten
   if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nblk * blk * 128 * NH));
   __syncwarp();
   if (lane < nblk) {
-    const int b = sbt[row0 / blk + lane - b0];
+    const int b = c.bt[(long long)s * c.max_blocks + row0 / blk + lane];
     const int z = (int)((long long)l * c.nblocks + b);
 #pragma unroll
     for (int hh = 0; hh < NH; ++hh) tma_load_4d(dst + hh * TR * 128 + lane * blk * 128, map, 64 * hh, g, 0, z, full);
   }
 }
 
+// Mean and M2 per head over one tile's scores by the consumer warps only
+// (named barrier 1), shifted by the tile's first score as head_mean_m2.
+template <int G>
+__device__ __forceinline__ void tile_mean_m2(const float *scores, int stride, int n, float *red, int nthreads,
+                                             float (&mu)[G], float (&m2)[G]) {
+  float v[G], sh[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    v[h] = 0.f;
+    sh[h] = scores[h * stride];
+  }
+  for (int i = threadIdx.x; i < n; i += nthreads) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) v[h] += scores[h * stride + i] - sh[h];
+  }
+  group_sum<G>(v, red, nthreads);
+  float md[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    md[h] = v[h] / (float)n;
+    mu[h] = sh[h] + md[h];
+    v[h] = 0.f;
+  }
+  for (int i = threadIdx.x; i < n; i += nthreads) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float dl = (scores[h * stride + i] - sh[h]) - md[h];
+      v[h] = fmaf(dl, dl, v[h]);
+    }
+  }
+  group_sum<G>(v, red, nthreads);
+#pragma unroll
+  for (int h = 0; h < G; ++h) m2[h] = v[h];
+}
+
 // Tensor-core variant of score_tiles_kernel for bf16 caches with rotate-half
-// bands: each stage of TR rows holds TR / 16 key tiles of 16, which the
-// consumer warps score with score_tile_mma (for d = 128 two groups of 4 warps
-// take alternate stages; the empty barrier then counts the 4 warps of a group).
+// bands.  A CTA covers kTilesPerCta consecutive tiles of one unit: the weights
+// are built once, the producer warp streams the CTA's whole row range through
+// the ring, and the 8 consumer warps score 16-key tiles of each stage with
+// score_tile_mma (for d = 128 two groups of 4 warps take alternate stages; the
+// empty barrier then counts the 4 warps of a group).  At the end of each tile
+// the consumer warps alone (named barrier) write its raw scores and (mean, M2)
+// while the producer keeps loading the next tile.
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __grid_constant__ TileArgs a) {
   constexpr int F = D / 2;
   constexpr int TR = kStageBytes / (2 * D);
   constexpr int SPS = TR / 16;                    // key tiles per stage
   constexpr int GROUPS = kConsumerWarps / SPS;    // warp groups taking alternate stages
+  constexpr int TK = tile_keys_for(G), TS = tile_stride_for(G);
+  constexpr int SPT = TK / TR;                    // stages per tile
+  constexpr int NC = kConsumerWarps * 32;
   extern __shared__ __align__(1024) char smem[];
   const TileLayout lay(G, F);
   const Pipe pipe = make_pipe(smem, lay.bars);
@@ -393,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
   float *red = reinterpret_cast<float *>(smem + lay.red);
   float *scores = reinterpret_cast<float *>(smem + lay.scores);
   const CacheView &c = a.c;
-  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, u = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u = blockIdx.y;
   const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
   if (timed_out()) return;
   const int N = c.seq_len[s];
@@ -403,12 +441,11 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
     return;
   }
   if (a.skip_small && N <= a.budget) return;
-  constexpr int TK = tile_keys_for(G), TS = tile_stride_for(G);
-  const int i0 = tile * TK;
+  const int tile0 = blockIdx.x * kTilesPerCta;
+  const int i0 = tile0 * TK;
   if (i0 >= N) return;
-  const int n = min(TK, N - i0);
-  int *sbt = reinterpret_cast<int *>(smem + lay.sbt);
-  if (!c.blocks_ok(s, n, i0, c.tm_ok ? sbt : nullptr)) {
+  const int n = min(kTilesPerCta * TK, N - i0);   // rows of this CTA
+  if (!c.blocks_ok(s, n, i0)) {
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
@@ -423,18 +460,18 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
   }
   build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc, a.phase + (long long)s * F);
   __syncthreads();
-  const int ntiles = (n + TR - 1) / TR;
+  const int nst = (n + TR - 1) / TR;   // stages of this CTA
   const long long urow0 = (long long)u * c.cap;   // dense: row of slot 0 in the 2-D view
   if (warp == kProducerWarp) {
     int t = 0;
-    for (; t < ntiles; ++t) {
+    for (; t < nst; ++t) {
       const int st = t % kStages;
       if (*pipe.fail || (t >= kStages && !mbar_wait(&pipe.empty[st], (uint32_t)(((t / kStages) - 1) & 1)))) {
         *pipe.fail = 1;
         break;
       }
-      produce_stage_sw<D>(c, &a.ks, sbt, c.paged() ? i0 / c.block : 0, l, s, g, urow0, i0 + t * TR,
-                          min(TR, n - t * TR), pipe.ring + st * kStageBytes, &pipe.full[st], lane);
+      produce_stage_sw<D>(c, &a.ks, l, s, g, urow0, i0 + t * TR, min(TR, n - t * TR),
+                          pipe.ring + st * kStageBytes, &pipe.full[st], lane);
     }
     if (lane == 0) *pipe.issued = t;
   } else {
@@ -442,13 +479,33 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
     load_mma_weights<D, G>(w, wts);
     const int grp = warp / SPS, sub = warp % SPS;
     const uint32_t ring = smem_u32(pipe.ring);
-    for (int t = grp; t < ntiles; t += GROUPS) {
-      const int st = t % kStages;
-      if (!*pipe.fail && !mbar_wait(&pipe.full[st], (uint32_t)((t / kStages) & 1))) *pipe.fail = 1;
-      score_tile_mma<D, G, TR>(ring + st * kStageBytes, 16 * sub, min(TR, n - t * TR), t * TR, scores,
-                               TS, w);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pipe.empty[st]);
+    for (int tt = 0; tt * SPT < nst; ++tt) {   // tiles of this CTA
+      const int tbeg = tt * SPT, tend = min(nst, tbeg + SPT);
+      for (int t = tbeg + (grp - tbeg % GROUPS + GROUPS) % GROUPS; t < tend; t += GROUPS) {
+        const int st = t % kStages;
+        if (!*pipe.fail && !mbar_wait(&pipe.full[st], (uint32_t)((t / kStages) & 1))) *pipe.fail = 1;
+        score_tile_mma<D, G, TR>(ring + st * kStageBytes, 16 * sub, min(TR, n - t * TR), (t - tbeg) * TR,
+                                 scores, TS, w);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pipe.empty[st]);
+      }
+      named_sync(1, NC);   // the tile's scores are in shared memory
+      const int tn = min(TK, n - tbeg * TR);
+      const int ti0 = i0 + tbeg * TR;
+      if (!*pipe.fail) {
+        for (int i = tid; i < tn; i += NC) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * a.raw_stride + ti0 + i] = scores[h * TS + i];
+        }
+        float mu[G], m2[G];
+        tile_mean_m2<G>(scores, TS, tn, red, NC, mu, m2);
+        if (tid == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            a.part[((long long)u * a.ntiles + tile0 + tt) * G + h] = make_float2(mu[h], m2[h]);
+        }
+      }
+      named_sync(1, NC);   // scores may be overwritten by the next tile
     }
   }
   __syncthreads();
@@ -461,18 +518,6 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
       }
     }
     __syncthreads();
-    return;
-  }
-  for (int i = tid; i < n; i += nt) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * a.raw_stride + i0 + i] = scores[h * TS + i];
-  }
-  float mu[G], m2[G];
-  head_mean_m2<G>(scores, TS, n, red, mu, m2);
-  if (tid == 0) {
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-      a.part[((long long)u * a.ntiles + tile) * G + h] = make_float2(mu[h], m2[h]);
   }
 }
 
@@ -984,7 +1029,8 @@ static tri_status run_tiles(const TileArgs &a, int64_t units, cudaStream_t st) {
     if (a.mma_ok) {
       auto k = score_tiles_mma_kernel<D, G>;
       if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
-      k<<<dim3((unsigned)a.ntiles, (unsigned)units), kThreads, lay.total, st>>>(a);
+      const unsigned ctas = (unsigned)((a.ntiles + kTilesPerCta - 1) / kTilesPerCta);
+      k<<<dim3(ctas, (unsigned)units), kThreads, lay.total, st>>>(a);
       return launch_result();
     }
   }

@@ -25,6 +25,7 @@ constexpr int kMaxCompactStages = 13;           // and at most (bounded by share
 // sit in shared memory next to the 64 KB ring; 1024 keys for G = 8 keep two CTAs
 // per SM.
 __host__ __device__ constexpr int tile_keys_for(int G) { return G >= 8 ? 1024 : 2048; }
+constexpr int kTilesPerCta = 4;   // tiles of one unit per CTA in the tensor-core score kernel
 constexpr int kSelThreads = 512;                // CTA size of the select/compact kernel
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // bounded device waits: 2 s
 
@@ -256,6 +257,37 @@ __device__ __forceinline__ void block_sum(float (&v)[G], float *red) {
     v[h] = t;
   }
   __syncthreads();
+}
+
+// Barrier over the first n threads of the CTA (n a multiple of 32) on named
+// barrier `id` (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// block_sum over the first nthreads threads only, synchronised on named barrier 1.
+template <int G>
+__device__ __forceinline__ void group_sum(float (&v)[G], float *red, int nthreads) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = nthreads >> 5;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float x = v[h];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    v[h] = x;
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) red[warp * G + h] = v[h];
+  }
+  named_sync(1, nthreads);
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float t = 0.f;
+    for (int w = 0; w < nw; ++w) t += red[w * G + h];
+    v[h] = t;
+  }
+  named_sync(1, nthreads);
 }
 
 // Exclusive prefix sum of one int per thread across the CTA; *total receives

@@ -58,16 +58,14 @@ struct CacheView {
     return (((long long)l * nblocks + b) * block + (i % block)) * Hkv + g;
   }
   // Checks every block id that rows [row0, row0 + n) of sequence s touch
-  // (CTA-wide; every thread gets the answer).  If `keep` is given, the ids are
-  // also stored there (keep[b - row0 / block]) for the copy issue path.
-  __device__ bool blocks_ok(int s, int n, int row0 = 0, int *keep = nullptr) const {
+  // (CTA-wide; every thread gets the answer).
+  __device__ bool blocks_ok(int s, int n, int row0 = 0) const {
     if (bt == nullptr) return true;
     const int b0 = row0 / block, nb = (row0 + n + block - 1) / block;
     int bad = 0;
     for (int b = b0 + threadIdx.x; b < nb; b += blockDim.x) {
       const int id = bt[(long long)s * max_blocks + b];
       bad |= (id < 0 || id >= nblocks);
-      if (keep != nullptr) keep[b - b0] = id;
     }
     return __syncthreads_or(bad) == 0;
   }
@@ -364,9 +362,9 @@ __device__ __forceinline__ void pipe_init(const Pipe &p) {
 // of the last block past nrows are loaded too, they exist).  Paged without: one
 // bulk copy per row.  Called by all 32 lanes of the producer warp.
 template <int RB>
-__device__ __forceinline__ void produce_stage(const CacheView &c, const CUtensorMap *tmk, const int *sbt,
-                                              int b0, int l, int s, int g, int row0, int nrows, char *dst,
-                                              uint64_t *full, int lane) {
+__device__ __forceinline__ void produce_stage(const CacheView &c, const CUtensorMap *tmk, int l, int s,
+                                              int g, int row0, int nrows, char *dst, uint64_t *full,
+                                              int lane) {
   if (!c.paged()) {
     if (lane == 0) {
       const uint32_t bytes = (uint32_t)nrows * (uint32_t)RB;
@@ -380,7 +378,7 @@ __device__ __forceinline__ void produce_stage(const CacheView &c, const CUtensor
     if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nblk * blk * RB));
     __syncwarp();
     if (lane < nblk) {
-      const int b = sbt[row0 / blk + lane - b0];
+      const int b = c.bt[(long long)s * c.max_blocks + row0 / blk + lane];
       tma_load_4d(dst + lane * blk * RB, tmk, 0, g, 0, (int)((long long)l * c.nblocks + b), full);
     }
     return;
@@ -401,8 +399,8 @@ __device__ __forceinline__ void produce_stage(const CacheView &c, const CUtensor
 // every thread of the CTA (kThreads); returns false (CTA-uniform, after a
 // barrier) if a wait gave up.  The caller initialised the pipe and synchronised.
 template <int D, int G, bool BF16>
-__device__ bool stream_and_score(const CacheView &c, const CUtensorMap *tmk, const int *sbt, int l, int s,
-                                 int g, int row_begin, int n, const Pipe &p, float *scores, int sstride,
+__device__ bool stream_and_score(const CacheView &c, const CUtensorMap *tmk, int l, int s, int g,
+                                 int row_begin, int n, const Pipe &p, float *scores, int sstride,
                                  const LaneWeights<G> &lw, bool inter) {
   using RG = RowGeom<D, BF16>;
   constexpr int TR = kStageBytes / RG::RB;
@@ -416,8 +414,8 @@ __device__ bool stream_and_score(const CacheView &c, const CUtensorMap *tmk, con
         *p.fail = 1;
         break;
       }
-      produce_stage<RG::RB>(c, tmk, sbt, row_begin / c.block, l, s, g, row_begin + t * TR,
-                            min(TR, n - t * TR), p.ring + st * kStageBytes, &p.full[st], lane);
+      produce_stage<RG::RB>(c, tmk, l, s, g, row_begin + t * TR, min(TR, n - t * TR),
+                            p.ring + st * kStageBytes, &p.full[st], lane);
     }
     if (lane == 0) *p.issued = t;
   } else {
