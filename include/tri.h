@@ -47,7 +47,9 @@
  *   - Conditions only visible on the device (seq_len[s] > cap, a block id out of
  *     range, an idx list that is not strictly increasing inside [0, N)) skip the
  *     affected unit and record the first error code in a device status word read
- *     by tri_get_device_status().  Device waits are bounded; a wait that gives
+ *     by tri_get_device_status().  A sequence skipped for a bad block id gets
+ *     new_len = N (nothing compressed); with seq_len > cap new_len is not
+ *     written.  Device waits are bounded; a wait that gives
  *     up records TRI_ERR_TIMEOUT, after which the kernels of this and later calls
  *     return without work until tri_clear_device_status().
  *   - No C++ exception crosses this ABI.

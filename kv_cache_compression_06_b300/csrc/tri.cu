@@ -146,19 +146,20 @@ __global__ void __launch_bounds__(kFusedThreads, (G <= 4 ? 2 : 1)) fused_kernel(
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
-  if (a.mode == 0) {
-    if (tid == 0 && a.new_len != nullptr && l == 0 && g == 0) a.new_len[s] = min(N, B);
-    if (N <= B) {
-      if (a.idx_out != nullptr)
-        for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = j < N ? j : -1;
-      return;
-    }
-  }
-  if (N == 0) return;
-  if (!c.blocks_ok(s, N)) {
-    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+  const bool len_writer = a.mode == 0 && tid == 0 && a.new_len != nullptr && l == 0 && g == 0;
+  if (a.mode == 0 && N <= B) {
+    if (len_writer) a.new_len[s] = N;
+    if (a.idx_out != nullptr)
+      for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = j < N ? j : -1;
     return;
   }
+  if (N == 0) return;
+  if (!c.blocks_ok(s, N)) {   // the sequence is skipped: its length stays N
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    if (len_writer) a.new_len[s] = N;
+    return;
+  }
+  if (len_writer) a.new_len[s] = B;
   const int ss = lay.sstride;
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 32);
@@ -718,16 +719,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
-  if (a.mode != 1 && tid == 0 && a.new_len != nullptr && l == 0 && g == 0) a.new_len[s] = min(N, B);
+  const bool len_writer = a.mode != 1 && tid == 0 && a.new_len != nullptr && l == 0 && g == 0;
   if (N <= B) {
+    if (len_writer) a.new_len[s] = N;
     if (a.mode != 2 && a.idx_out != nullptr)
       for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = j < N ? j : -1;
     return;
   }
-  if (a.mode != 1 && !c.blocks_ok(s, N)) {
+  if (a.mode != 1 && !c.blocks_ok(s, N)) {   // the sequence is skipped: its length stays N
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    if (len_writer) a.new_len[s] = N;
     return;
   }
+  if (len_writer) a.new_len[s] = B;
   if (tid == 0) {
     for (int st = 0; st < lay.nstages; ++st) {
       mbar_init(&cbars[st], 1);                       // K warp
