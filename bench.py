@@ -210,6 +210,17 @@ def _moved_rows(idx, seq_len, B):
     return int(torch.where(n > B, B - e0, torch.zeros_like(e0)).sum())
 
 
+def _moved_rows_holefill(idx, seq_len, B):
+    """Rows a hole-fill compaction moves: slots j < B whose row came from elsewhere."""
+    import torch
+    ii = idx.view(-1, B).long()
+    ar = torch.arange(B, device=ii.device)
+    L, S, Hkv = idx.shape[0], idx.shape[1], idx.shape[2]
+    n = seq_len.long().view(1, S, 1).expand(L, S, Hkv).reshape(-1)
+    moved = ((ii != ar) & (ii >= 0)).sum(dim=1)
+    return int(torch.where(n > B, moved, torch.zeros_like(moved)).sum())
+
+
 def run_b300(args, w):
     import torch
     import torch.distributed as dist
@@ -257,7 +268,8 @@ def run_b300(args, w):
             flush.fill_(1)
 
     def step():
-        tk.tri_compress_step(cache, stats, params, idx_out=idx, new_len=new_len, ws=ws, stream=stream)
+        tk.tri_compress_step(cache, stats, params, idx_out=idx, new_len=new_len, ws=ws, stream=stream,
+                             compact=args.compact)
 
     for _ in range(args.warmup):
         restore()
@@ -269,7 +281,7 @@ def run_b300(args, w):
     # compaction, over the units the step compresses (N > B)
     B, rb = w.budget, w.d * w.esize
     lens = [int(x) for x in data["seq_len"].tolist()]
-    M = _moved_rows(idx, data["seq_len"], B)
+    M = _moved_rows(idx, data["seq_len"], B) if args.compact == "ordered" else _moved_rows_holefill(idx, data["seq_len"], B)
     units = L * w.S * w.Hkv
     n_keys = L * w.Hkv * sum(lens)
     scored = L * w.Hkv * sum(n for n in lens if n > B)
@@ -339,7 +351,7 @@ def run_b300(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": _config(w, {"layers": L,
+        "config": _config(w, {"layers": L, "compaction": args.compact,
                               "l2": f"cache restored from a pristine {cache_bytes / 1e9:.3f} GB copy before every "
                                     "step" + (" plus a 256 MB L2 flush" if flush is not None else " (flushes L2)")
                                     + "; untimed",
@@ -380,6 +392,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="use only the first N layers (small case for ncu captures, or a layer group "
                          "of a workload whose full cache exceeds HBM)")
+    ap.add_argument("--compact", default="ordered", choices=["ordered", "holefill"],
+                    help="layout of the kept rows (default: ordered, the slot order of the kept keys)")
     ap.add_argument("--seqs", type=int, default=None,
                     help="use only N sequences (small case for ncu captures)")
     args = ap.parse_args()

@@ -83,7 +83,16 @@ typedef enum {
 
 typedef enum { TRI_F32 = 0, TRI_BF16 = 1 } tri_dtype;
 typedef enum { TRI_PAIR_HALF = 0, TRI_PAIR_INTERLEAVED = 1 } tri_pairing;
-typedef enum { TRI_COMPACT_ORDERED = 0 } tri_compact_mode;
+/* Layout of the B kept rows after compaction (both keep the same set):
+ *   TRI_COMPACT_ORDERED : slot j holds the j-th kept slot in ascending order
+ *                         (moves the kept rows past the first evicted slot);
+ *   TRI_COMPACT_HOLEFILL: kept slots below B stay where they are; the evicted
+ *                         slots below B, ascending, receive the kept slots at or
+ *                         above B, ascending (moves at most min(B, N - B) rows).
+ *                         Valid because a post-RoPE key carries its position in
+ *                         its phase and V rows move with their K rows; a caller
+ *                         that needs positions tracks them through idx_out. */
+typedef enum { TRI_COMPACT_ORDERED = 0, TRI_COMPACT_HOLEFILL = 1 } tri_compact_mode;
 
 /* KV cache description.
  * Dense (block_table == NULL): k and v are each [L][S][Hkv][cap][d] contiguous,
@@ -160,17 +169,22 @@ TRI_API tri_status tri_score(const tri_cache *cache, const tri_stats *stats, con
 TRI_API tri_status tri_select_topb(const tri_cache *cache, const float *agg, int budget, int32_t *idx,
                            void *ws, size_t ws_bytes, cudaStream_t stream);
 
-/* In-place ordered compaction: for every unit with N > budget, row j of K and V
- * (j < budget) becomes row idx[u][j].  idx rows must be strictly increasing in
- * [0, N) (checked on the device: a bad row skips its unit and records
- * TRI_ERR_INVALID).  new_len: NULL or [S] int32 receiving min(N, budget); it
- * must not alias seq_len. */
+/* In-place compaction of every unit with N > budget to its kept slots
+ * idx[u][0..budget) (as tri_select_topb writes them: strictly increasing in
+ * [0, N), checked on the device: a bad row skips its unit and records
+ * TRI_ERR_INVALID).  ORDERED: row j of K and V becomes row idx[u][j];
+ * HOLEFILL: the hole-fill layout of those slots (see tri_compact_mode).
+ * new_len: NULL or [S] int32 receiving min(N, budget); it must not alias
+ * seq_len. */
 TRI_API tri_status tri_compact_kv(const tri_cache *cache, const int32_t *idx, int budget,
                           tri_compact_mode mode, int32_t *new_len, cudaStream_t stream);
 
 /* The fused step: score -> GQA z/max -> top-B -> in-place compaction for every
  * unit with N > budget (units with N <= budget untouched).
- * idx_out: NULL or [L][S][Hkv][budget] int32 as tri_select_topb writes it.
+ * idx_out: NULL or [L][S][Hkv][budget] int32: the original slot of the row now
+ * at each slot j < budget (ORDERED: the kept slots ascending, as
+ * tri_select_topb writes them; HOLEFILL: j for kept slots below B, the mover
+ * for each hole).
  * new_len: NULL or [S] int32 (min(N, budget)); must not alias seq_len. */
 TRI_API tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
                              const tri_params *params, tri_compact_mode mode, int32_t *idx_out,

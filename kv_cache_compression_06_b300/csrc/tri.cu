@@ -92,6 +92,7 @@ struct FusedArgs {
   int Hq;
   const int *t;
   int budget, mode, inter, capp;   // mode 0: compress, 1: score only
+  int holefill;                    // compaction layout: 0 ordered, 1 hole-fill
   float *agg, *raw;
   int *idx_out, *new_len;
   StepConst sc;
@@ -198,6 +199,11 @@ __global__ void __launch_bounds__(kFusedThreads, (G <= 4 ? 2 : 1)) fused_kernel(
   int ntie;
   const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
   const int e0 = build_kept_chunked(keys, N, B, T, ntie, idxs, sm);
+  if (a.holefill) {   // keys are dead: their 4N bytes hold the hole-fill bookkeeping
+    holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), sm,
+                  a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
+    return;
+  }
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
   // The ring was last read by generic loads (scoring); TMA writes it next.
@@ -610,6 +616,7 @@ struct SCArgs {
   TmaMaps maps;
   CacheView c;
   int G, budget, mode, ntiles, capp, bcap;   // mode 0: from raw (+compact), 1: from agg, 2: compact idx
+  int holefill;                              // compaction layout (modes 0, 2): 0 ordered, 1 hole-fill
   const float *raw;     // mode 0: workspace [(u*G + h)*capp + i], rows 16-byte aligned
   const float2 *part;
   const float *agg;
@@ -700,7 +707,7 @@ __device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *
 
 __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __grid_constant__ SCArgs a) {
   extern __shared__ __align__(1024) char smem[];
-  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap);
+  const SCLayout lay(a.capp, a.bcap);
   char *ring = smem;
   uint64_t *cbars = reinterpret_cast<uint64_t *>(smem + lay.bars);
   uint32_t *hist = reinterpret_cast<uint32_t *>(smem + lay.hist);
@@ -752,6 +759,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
       if (tid == 0) set_status(TRI_ERR_INVALID);
       return;
     }
+    if (a.holefill) {
+      holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), sm, nullptr);
+      return;
+    }
     for (int j = tid; j < B; j += nt)
       if (idxs[j] != j) atomicMin(&sm[56], j);
     __syncthreads();
@@ -779,6 +790,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
   int ntie;
   const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
   const int e0 = build_kept(keys, N, B, T, ntie, idxs, sm);
+  if (a.mode == 0 && a.holefill) {   // keys are dead: their region holds the hole-fill bookkeeping
+    holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), sm,
+                  a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
+    return;
+  }
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
   if (a.mode == 0) {
@@ -1069,7 +1085,7 @@ static tri_status run_tiles(const TileArgs &a, int64_t units, cudaStream_t st) {
   }()
 
 static tri_status run_select_compact(const SCArgs &a, int64_t units, cudaStream_t st) {
-  const SCLayout lay(a.mode == 2 ? 0 : a.capp, a.bcap);
+  const SCLayout lay(a.capp, a.bcap);
   if (lay.total > kMaxSmem) return TRI_ERR_UNSUPPORTED;
   if (set_smem(select_compact_kernel, lay.total) != TRI_OK) return TRI_ERR_CUDA;
   select_compact_kernel<<<(unsigned)units, kSelThreads, lay.total, st>>>(a);
@@ -1254,7 +1270,7 @@ tri_status tri_compact_kv(const tri_cache *cache, const int32_t *idx, int budget
   tri_status e;
   if ((e = check_cache(cache, true, true)) != TRI_OK) return e;
   if (idx == nullptr || budget < 1) return TRI_ERR_INVALID;
-  if (mode != TRI_COMPACT_ORDERED) return TRI_ERR_UNSUPPORTED;
+  if (mode != TRI_COMPACT_ORDERED && mode != TRI_COMPACT_HOLEFILL) return TRI_ERR_UNSUPPORTED;
   if (new_len != nullptr && new_len == cache->seq_len) return TRI_ERR_INVALID;
   SCArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -1262,7 +1278,8 @@ tri_status tri_compact_kv(const tri_cache *cache, const int32_t *idx, int budget
   make_maps(cache, &a.c, &a.maps);
   a.budget = budget;
   a.mode = 2;
-  a.capp = 0;
+  a.holefill = mode == TRI_COMPACT_HOLEFILL;
+  a.capp = a.holefill ? round32(cache->cap) : 0;   // hole-fill bookkeeping: < 4 N bytes in the keys region
   a.bcap = bcap_of(cache, budget);
   a.idx_in = idx;
   a.new_len = new_len;
@@ -1276,7 +1293,7 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   if ((e = check_cache(cache, true, true)) != TRI_OK) return e;
   if ((e = check_stats(cache, stats)) != TRI_OK) return e;
   if ((e = check_params(params)) != TRI_OK) return e;
-  if (mode != TRI_COMPACT_ORDERED) return TRI_ERR_UNSUPPORTED;
+  if (mode != TRI_COMPACT_ORDERED && mode != TRI_COMPACT_HOLEFILL) return TRI_ERR_UNSUPPORTED;
   if (new_len != nullptr && new_len == cache->seq_len) return TRI_ERR_INVALID;
   const int G = stats->Hq / cache->Hkv;
   const bool bf16 = cache->dtype == TRI_BF16;
@@ -1284,6 +1301,7 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   if (fused_fits(cache, G)) {
     FusedArgs a = fused_args(cache, stats, params);
     a.mode = 0;
+    a.holefill = mode == TRI_COMPACT_HOLEFILL;
     a.idx_out = idx_out;
     a.new_len = new_len;
     return TRI_DISPATCH(run_fused, cache->d, G, bf16, a, units, stream);
@@ -1297,6 +1315,7 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   sa.G = G;
   sa.budget = params->budget;
   sa.mode = 0;
+  sa.holefill = mode == TRI_COMPACT_HOLEFILL;
   sa.ntiles = ntiles_of(cache, G);
   sa.capp = round32(cache->cap);
   sa.bcap = bcap_of(cache, params->budget);
@@ -1322,7 +1341,7 @@ tri_status tri_compress_step_static_scratch(const tri_cache *cache, const tri_st
                                             cudaStream_t stream) {
   tri_status e;
   if ((e = check_cache(cache, true, true)) != TRI_OK) return e;
-  if (mode != TRI_COMPACT_ORDERED) return TRI_ERR_UNSUPPORTED;
+  if (mode != TRI_COMPACT_ORDERED && mode != TRI_COMPACT_HOLEFILL) return TRI_ERR_UNSUPPORTED;
   size_t need = 0;
   if ((e = tri_workspace_bytes(cache, stats, params, &need)) != TRI_OK) return e;
   if (need == 0) return tri_compress_step(cache, stats, params, mode, idx_out, new_len, nullptr, 0, stream);

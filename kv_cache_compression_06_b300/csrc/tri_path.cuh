@@ -889,4 +889,75 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
   return ok;
 }
 
+// ---------------------------------------------------------------- hole-fill compaction (a5, alternative)
+// Hole-fill layout of unit (l, s, g) from its ascending kept list idx[0..B):
+// kept slots below B stay; the evicted slots below B (holes, ascending) receive
+// the kept slots at or above B (movers, ascending), the k-th hole the k-th
+// mover.  Sources (>= B) and destinations (< B) are disjoint, so every row copy
+// is independent: all threads of the CTA copy 16-byte pieces, four loads in
+// flight per thread before their stores.  `work` (shared, >= 4 N bytes, 16-byte
+// aligned, dead by now) holds one flag byte per slot below B, then the hole
+// list.  out (global, may be null) receives the layout: out[j] = original slot
+// now at j.  sm: 40 ints for the scan.  Ends with a CTA barrier.
+__device__ __noinline__ void holefill_unit(const CacheView &c, int l, int s, int g, const int *idx, int B,
+                                           int N, char *work, int *sm, int *out) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  unsigned char *kept = reinterpret_cast<unsigned char *>(work);
+  int *holes = reinterpret_cast<int *>(work + ((B + 15) & ~15));
+  for (int j = tid; j < B; j += nt) kept[j] = 0;
+  __syncthreads();
+  for (int j = tid; j < B; j += nt) {
+    const int v = idx[j];
+    if (v < B) kept[v] = 1;
+  }
+  __syncthreads();
+  // holes in slot order: each thread scans a contiguous chunk of slots
+  const int chunk = (B + nt - 1) / nt;
+  const int j0 = min(B, tid * chunk), j1 = min(B, j0 + chunk);
+  int nh = 0;
+  for (int j = j0; j < j1; ++j) nh += kept[j] == 0;
+  int total;
+  int r = block_excl_scan(nh, sm, &total);
+  const int P = B - total;   // kept slots below B; movers are idx[P..B)
+  for (int j = j0; j < j1; ++j) {
+    if (kept[j]) {
+      if (out != nullptr) out[j] = j;
+    } else {
+      holes[r] = j;
+      if (out != nullptr) out[j] = idx[P + r];
+      ++r;
+    }
+  }
+  __syncthreads();
+  // copy mover rows into the holes (K and V): piece q of the 2 * ppr pieces of
+  // pair k (ppr = 16-byte pieces per row, a power of two) is K piece q for
+  // q < ppr, else V piece q - ppr; each lane keeps 4 pieces in flight
+  const int ppr = c.rb / 16, lp = __ffs(2 * ppr) - 1;
+  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  const int pieces = total << lp;
+  for (int base = warp * 128; base < pieces; base += nw * 128) {
+    uint4 v[4];
+    char *dst[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int q = base + e * 32 + lane;
+      dst[e] = nullptr;
+      if (q < pieces) {
+        const int k = q >> lp, rem = q & (2 * ppr - 1);
+        const int tsr = rem >= ppr, col = rem & (ppr - 1);
+        char *tb = tsr ? c.v : c.k;
+        const long long so = c.row_off(l, s, g, idx[P + k]), dof = c.row_off(l, s, g, holes[k]);
+        if (so >= 0 && dof >= 0) {
+          v[e] = *reinterpret_cast<const uint4 *>(tb + so + col * 16);
+          dst[e] = tb + dof + col * 16;
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (dst[e] != nullptr) *reinterpret_cast<uint4 *>(dst[e]) = v[e];
+  }
+  __syncthreads();
+}
+
 }  // namespace tri

@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(_HERE, "libtri.so")
 TRI_OK, TRI_ERR_INVALID, TRI_ERR_CUDA, TRI_ERR_UNSUPPORTED, TRI_ERR_WORKSPACE, TRI_ERR_TIMEOUT, TRI_ERR_BOUNDS = range(7)
 TRI_F32, TRI_BF16 = 0, 1
 TRI_PAIR_HALF, TRI_PAIR_INTERLEAVED = 0, 1
-TRI_COMPACT_ORDERED = 0
+TRI_COMPACT_ORDERED, TRI_COMPACT_HOLEFILL = 0, 1
+_COMPACT = {"ordered": TRI_COMPACT_ORDERED, "holefill": TRI_COMPACT_HOLEFILL}
 
 EXPORTED = ("tri_calibrate_stats", "tri_workspace_bytes", "tri_score", "tri_select_topb",
             "tri_compact_kv", "tri_compress_step", "tri_get_device_status",
@@ -258,10 +259,11 @@ def tri_select_topb(cache: KVCache, agg: torch.Tensor, budget: int, idx: Optiona
 
 
 def tri_compact_kv(cache: KVCache, idx: torch.Tensor, budget: int, new_len: Optional[torch.Tensor] = None,
-                   stream=None) -> Optional[torch.Tensor]:
-    """In-place ordered compaction of K and V to the rows idx (per unit)."""
+                   stream=None, compact: str = "ordered") -> Optional[torch.Tensor]:
+    """In-place compaction of K and V to the kept slots idx (per unit, ascending);
+    compact = 'ordered' or 'holefill' (layout, see include/tri.h)."""
     c = cache.to_c()
-    st = lib().tri_compact_kv(ctypes.byref(c), _ptr(idx), int(budget), TRI_COMPACT_ORDERED, _ptr(new_len),
+    st = lib().tri_compact_kv(ctypes.byref(c), _ptr(idx), int(budget), _COMPACT[compact], _ptr(new_len),
                               _stream(stream))
     _check("tri_compact_kv", st)
     return new_len
@@ -269,13 +271,14 @@ def tri_compact_kv(cache: KVCache, idx: torch.Tensor, budget: int, new_len: Opti
 
 def tri_compress_step(cache: KVCache, stats: Stats, params: Params, idx_out: Optional[torch.Tensor] = None,
                       new_len: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
-                      stream=None):
-    """The fused step (score -> z/max -> top-B -> compact) on every unit with N > B."""
+                      stream=None, compact: str = "ordered"):
+    """The fused step (score -> z/max -> top-B -> compact) on every unit with N > B;
+    compact = 'ordered' or 'holefill' (layout, see include/tri.h)."""
     if ws is None:
         ws = workspace(cache, stats, params)
     c, s = cache.to_c(), stats.to_c()
     p, _keep = params.to_c()
-    st = lib().tri_compress_step(ctypes.byref(c), ctypes.byref(s), ctypes.byref(p), TRI_COMPACT_ORDERED,
+    st = lib().tri_compress_step(ctypes.byref(c), ctypes.byref(s), ctypes.byref(p), _COMPACT[compact],
                                  _ptr(idx_out), _ptr(new_len), _ptr(ws), 0 if ws is None else ws.numel(),
                                  _stream(stream))
     _check("tri_compress_step", st)

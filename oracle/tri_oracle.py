@@ -42,7 +42,9 @@ Where the pages are silent or garbled, the readings taken here are:
   * z-score with the population standard deviation over all N keys of the unit,
     sigma = 0 gives z = 0; aggregation = max over the G query heads of a KV head;
   * top-B: order by (score descending, slot ascending), NaN lowest, N <= B keeps all;
-  * compaction: stable, kept rows to slots 0..B-1 in ascending original slot.
+  * compaction: stable, kept rows to slots 0..B-1 in ascending original slot;
+    the hole-fill alternative (holefill_layout) keeps the same set in place
+    below B and fills the evicted slots below B with the kept slots above.
 """
 from __future__ import annotations
 
@@ -199,6 +201,24 @@ def compact(x: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return np.asarray(x)[np.asarray(idx, dtype=np.int64)]
 
 
+def holefill_layout(kept: np.ndarray, B: int) -> np.ndarray:
+    """Hole-fill compaction layout (an alternative to the ordered one; the pages
+    fix only that the top-B keys are kept, W3-PRUNE).  kept: the ascending kept
+    slots (len B).  Kept slots below B stay where they are; the evicted slots
+    below B (the holes, ascending) receive the kept slots at or above B (the
+    movers, ascending), the k-th hole the k-th mover.  Returns src[j], the
+    original slot of the row that ends at slot j, for j < B."""
+    kept = np.asarray(kept, dtype=np.int64)
+    assert kept.shape[0] == B
+    inside = kept[kept < B]
+    movers = kept[kept >= B]
+    holes = np.setdiff1d(np.arange(B), inside)
+    assert holes.shape[0] == movers.shape[0]
+    src = np.arange(B, dtype=np.int64)
+    src[holes] = movers
+    return src
+
+
 # ----------------------------------------------------------------------------
 # One unit (sequence, layer, KV head) end to end
 # ----------------------------------------------------------------------------
@@ -211,7 +231,11 @@ def compress_unit(center, R, m, k_post, v, pos, t, offsets, theta, B, pairing="h
     s = key_scores(center, R, m, k_post, pos, t, offsets, theta, pairing)
     a = gqa_aggregate(s)
     idx = select_topb(a, B)
-    return {"s": s, "a": a, "idx": idx, "k": compact(k_post, idx), "v": compact(v, idx)}
+    out = {"s": s, "a": a, "idx": idx, "k": compact(k_post, idx), "v": compact(v, idx)}
+    if idx.shape[0] == B and k_post.shape[0] > B:
+        hf = holefill_layout(idx, B)
+        out.update(hf_src=hf, hf_k=compact(k_post, hf), hf_v=compact(v, hf))
+    return out
 
 
 def paged_logical_rows(pool, block_table_row, g, n, block=16):

@@ -115,3 +115,57 @@ def sample_units(w, L, n, seed):
     units.add((L - 1, int(np.argmax(lens)), w.Hkv - 1))
     units.add((0, int(np.argmin(lens)), 0))
     return sorted(units)
+
+
+def run_and_check_holefill(w, data, units, dev):
+    """Hole-fill layout through tri_compress_step and tri_compact_kv: the kept
+    set matches the oracle (tie band), the layout is the oracle's hole-fill
+    layout of the GPU's own kept set, every row is bit-exact, and the fused and
+    unfused paths agree."""
+    cache, stats, params = setup(w, data, dev)
+    pristine = {}
+    for (li, s, g) in units:
+        pristine[(li, s, g)] = (unit_rows(w, data, li, s, g, "k").double().cpu().numpy(),
+                                unit_rows(w, data, li, s, g, "v").double().cpu().numpy())
+    L = data["k"].shape[0]
+    agg = torch.zeros((L, w.S, w.Hkv, w.cap), dtype=torch.float32, device=dev)
+    tk.tri_score(cache, stats, params, agg=agg)
+    idx_sel = tk.tri_select_topb(cache, agg, w.budget)
+    k_copy, v_copy = cache.k.clone(), cache.v.clone()
+    idx = torch.full((L, w.S, w.Hkv, w.budget), -7, dtype=torch.int32, device=dev)
+    new_len = torch.zeros(w.S, dtype=torch.int32, device=dev)
+    tk.tri_compress_step(cache, stats, params, idx_out=idx, new_len=new_len, compact="holefill")
+    other = tk.KVCache(k_copy, v_copy, cache.seq_len, Hkv=w.Hkv, block_table=cache.block_table, block=w.block)
+    tk.tri_compact_kv(other, idx_sel, w.budget, compact="holefill")
+    torch.cuda.synchronize()
+    assert tk.tri_get_device_status() == 0
+    ostats = {}
+    for (li, s, g) in units:
+        if li not in ostats:
+            ostats[li] = O.calibrate(data["q_pre"][li].double().cpu().numpy(), w.pairing)
+        kr, vr = pristine[(li, s, g)]
+        N = kr.shape[0]
+        ref = H.oracle_unit(w, ostats[li], kr, vr, g, int(data["t"][s]))
+        gi = idx[li, s, g].cpu().numpy().astype(np.int64)
+        gsel = idx_sel[li, s, g].cpu().numpy().astype(np.int64)
+        assert int(new_len[s]) == min(N, w.budget)
+        if N <= w.budget:
+            H.check_kept(gi, ref["idx"], ref["a"], w.budget)
+            continue
+        assert np.array_equal(np.sort(gi), gsel), "fused and unfused kept sets differ"
+        H.check_kept(gsel, ref["idx"], ref["a"], w.budget)
+        assert np.array_equal(gi, O.holefill_layout(gsel, w.budget)), "not the hole-fill layout"
+        kd = {"k": cache.k, "v": cache.v}
+        k_after = unit_rows(w, {**data, **kd}, li, s, g, "k").double().cpu().numpy()
+        v_after = unit_rows(w, {**data, **kd}, li, s, g, "v").double().cpu().numpy()
+        np.testing.assert_array_equal(k_after[: w.budget], kr[gi])
+        np.testing.assert_array_equal(v_after[: w.budget], vr[gi])
+        if np.array_equal(gsel, ref["idx"]):
+            assert np.array_equal(gi, ref["hf_src"])
+            np.testing.assert_array_equal(k_after[: w.budget], ref["hf_k"])
+            np.testing.assert_array_equal(v_after[: w.budget], ref["hf_v"])
+        od = {"k": other.k, "v": other.v}
+        np.testing.assert_array_equal(unit_rows(w, {**data, **od}, li, s, g, "k").double().cpu().numpy()[: w.budget],
+                                      k_after[: w.budget])
+        np.testing.assert_array_equal(unit_rows(w, {**data, **od}, li, s, g, "v").double().cpu().numpy()[: w.budget],
+                                      v_after[: w.budget])

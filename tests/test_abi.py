@@ -115,7 +115,7 @@ def test_null_outputs_and_aliasing_rejected():
     assert L.tri_select_topb(ctypes.byref(c), None, 4, FAKE, None, 0, None) == T.TRI_ERR_INVALID
     assert L.tri_select_topb(ctypes.byref(c), FAKE, 0, FAKE, None, 0, None) == T.TRI_ERR_INVALID
     assert L.tri_compact_kv(ctypes.byref(c), None, 4, 0, None, None) == T.TRI_ERR_INVALID
-    assert L.tri_compact_kv(ctypes.byref(c), FAKE, 4, 1, None, None) == T.TRI_ERR_UNSUPPORTED
+    assert L.tri_compact_kv(ctypes.byref(c), FAKE, 4, 7, None, None) == T.TRI_ERR_UNSUPPORTED   # no such layout
     # new_len aliasing seq_len would race with units still reading N
     assert L.tri_compact_kv(ctypes.byref(c), FAKE, 4, 0, FAKE, None) == T.TRI_ERR_INVALID
     assert L.tri_compress_step(ctypes.byref(c), ctypes.byref(s), ctypes.byref(p), 0, None, FAKE, None, 0,

@@ -77,3 +77,19 @@ def test_all_zero_keys_tie_everywhere(n_keys):
     # the zero unit must keep exactly slots 0..B-1: no difference, even in the tie band
     assert C.run_and_check(w, data, [(0, 0, 1)], DEV) == 0
     C.run_and_check(w, generate(w, device=DEV), [(0, 0, 0)], DEV)
+
+
+HOLEFILL_CASES = [
+    W("hf_fused_g4", Hq=8, n_range=(600, 1900), budget=700),
+    W("hf_fused_paged_g2_d64", Hq=4, d=64, n_range=(700, 2500), paged=True),
+    W("hf_long_mma_g4", Hq=8, n_range=(9000, 13000), budget=1024),
+    W("hf_long_mma_g8_paged", Hq=16, n_range=(12000, 16000), budget=1024, paged=True),
+    W("hf_long_cuda_f32", Hq=4, d=64, dtype="f32", n_range=(30000, 40000), budget=2048, S=2),
+]
+
+
+@pytest.mark.parametrize("w", HOLEFILL_CASES, ids=[w.name for w in HOLEFILL_CASES])
+def test_holefill_every_unit(w):
+    data = generate(w, device=DEV)
+    units = [(0, s, g) for s in range(w.S) for g in range(w.Hkv)]
+    C.run_and_check_holefill(w, data, units, DEV)

@@ -43,3 +43,8 @@ def test_qwen3_32b_paged_sampled_units_layer_subset():
     generated (each from its own seed, identical to the full workload's)."""
     w = WORKLOADS["qwen3_32b_64l_b64_paged"]
     C.run_and_check(w, generate(w, device=DEV, layers=[0, 37]), C.sample_units(w, 2, 6, 5), DEV)
+
+
+def test_qwen3_8b_full_step_holefill_sampled_units():
+    w = WORKLOADS["qwen3_8b_36l_b16_n2176"]
+    C.run_and_check_holefill(w, generate(w, device=DEV, layers=list(range(8))), C.sample_units(w, 8, 24, 6), DEV)

@@ -284,3 +284,38 @@ def test_paged_logical_rows_match_dense_scatter():
         pool[table[j // block], j % block] = dense[:, j]
     for g in range(Hkv):
         np.testing.assert_array_equal(O.paged_logical_rows(pool, table, g, n, block), dense[g])
+
+
+# ---------------------------------------------------------------- hole-fill layout
+def _holefill_brute(kept, B):
+    """Move by move: walk the slots below B in order; each evicted one takes
+    the next kept slot at or above B."""
+    kept = set(int(i) for i in kept)
+    movers = iter(sorted(i for i in kept if i >= B))
+    out = []
+    for j in range(B):
+        out.append(j if j in kept else next(movers))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_holefill_layout_matches_move_by_move_and_keeps_the_set(seed):
+    rng = np.random.default_rng(100 + seed)
+    N = int(rng.integers(2, 60))
+    B = int(rng.integers(1, N))
+    kept = np.sort(rng.choice(N, size=B, replace=False))
+    src = O.holefill_layout(kept, B)
+    assert src.tolist() == _holefill_brute(kept, B)
+    assert sorted(src.tolist()) == kept.tolist()                 # same kept set as the ordered layout
+    inside = kept[kept < B]
+    assert np.all(src[inside] == inside)                         # kept slots below B do not move
+    assert int(np.sum(src != np.arange(B))) == int(np.sum(kept >= B))   # one move per kept slot >= B
+
+
+def test_holefill_rows_and_unit_output():
+    rng = np.random.default_rng(7)
+    x = rng.normal(size=(12, 3))
+    kept = np.array([0, 2, 3, 7, 9, 11])
+    src = O.holefill_layout(kept, 6)
+    assert src.tolist() == [0, 7, 2, 3, 9, 11]
+    np.testing.assert_array_equal(O.compact(x, src), x[[0, 7, 2, 3, 9, 11]])
