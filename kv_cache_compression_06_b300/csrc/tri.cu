@@ -93,6 +93,9 @@ struct FusedArgs {
   const int *t;
   int budget, mode, inter, capp;   // mode 0: compress, 1: score only
   int holefill;                    // compaction layout: 0 ordered, 1 hole-fill
+  int mma_ok;                      // host only: try the tensor-core variant
+  const tri_cache *cache;          // host only: for that variant's tensor map
+  const tri_params *params;
   float *agg, *raw;
   int *idx_out, *new_len;
   StepConst sc;
@@ -526,6 +529,151 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
     }
     __syncthreads();
   }
+}
+
+// ---------------------------------------------------------------- fused short-unit kernel, tensor cores
+// fused_kernel with the tensor-core score of score_tiles_mma_kernel (bf16
+// caches, rotate-half bands): a producer warp streams the unit's K through the
+// ring with 128B-swizzled tensor copies, 8 consumer warps score 16-key tiles
+// with score_tile_mma into the unit's shared-memory scores; then every thread
+// runs the same z/max, select and compaction as fused_kernel.
+struct FusedMmaArgs {
+  CUtensorMap ks;   // 128B-swizzled K map (as TileArgs::ks)
+  FusedArgs f;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
+    fused_mma_kernel(const __grid_constant__ FusedMmaArgs A) {
+  const FusedArgs &a = A.f;
+  constexpr int F = D / 2;
+  constexpr int TR = kStageBytes / (2 * D);
+  constexpr int SPS = TR / 16;
+  constexpr int GROUPS = kConsumerWarps / SPS;
+  extern __shared__ __align__(1024) char smem[];
+  const FusedLayout lay(G, F, a.capp);
+  char *ring = smem;
+  const Pipe pipe = make_pipe(smem, lay.bars);
+  uint64_t *cbars = pipe.full + 2 * kStages;
+  float *wts = reinterpret_cast<float *>(smem + lay.wts);
+  float *red = reinterpret_cast<float *>(smem + lay.red);
+  uint32_t *hist = reinterpret_cast<uint32_t *>(smem + lay.hist);
+  int *sm = reinterpret_cast<int *>(smem + lay.sm);
+  float *scores = reinterpret_cast<float *>(smem + lay.scores);
+  int *idxs = reinterpret_cast<int *>(smem + lay.idx);
+
+  const CacheView &c = a.c;
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  const int u = blockIdx.x;
+  const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
+  if (timed_out()) return;
+  const int N = c.seq_len[s];
+  const int B = a.budget;
+  if (N < 0 || N > c.cap) {
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  const bool len_writer = a.mode == 0 && tid == 0 && a.new_len != nullptr && l == 0 && g == 0;
+  if (a.mode == 0 && N <= B) {
+    if (len_writer) a.new_len[s] = N;
+    if (a.idx_out != nullptr)
+      for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = j < N ? j : -1;
+    return;
+  }
+  if (N == 0) return;
+  if (!c.blocks_ok(s, N)) {   // the sequence is skipped: its length stays N
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    if (len_writer) a.new_len[s] = N;
+    return;
+  }
+  if (len_writer) a.new_len[s] = B;
+  const int ss = lay.sstride;
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&pipe.full[st], 1);
+      mbar_init(&pipe.empty[st], SPS);
+      mbar_init(&cbars[st], 1);
+    }
+    *pipe.fail = 0;
+    *pipe.issued = 0;
+    fence_mbar_init();
+  }
+  build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc);
+  __syncthreads();
+  const int nst = (N + TR - 1) / TR;
+  if (warp == kProducerWarp) {
+    int t = 0;
+    for (; t < nst; ++t) {
+      const int st = t % kStages;
+      if (*pipe.fail || (t >= kStages && !mbar_wait(&pipe.empty[st], (uint32_t)(((t / kStages) - 1) & 1)))) {
+        *pipe.fail = 1;
+        break;
+      }
+      produce_stage_sw<D>(c, &A.ks, l, s, g, (long long)u * c.cap, t * TR, min(TR, N - t * TR),
+                          ring + st * kStageBytes, &pipe.full[st], lane);
+    }
+    if (lane == 0) *pipe.issued = t;
+  } else {
+    MmaWeights<D, G> w;
+    load_mma_weights<D, G>(w, wts);
+    const int grp = warp / SPS, sub = warp % SPS;
+    const uint32_t ring_a = smem_u32(ring);
+    for (int t = grp; t < nst; t += GROUPS) {
+      const int st = t % kStages;
+      if (!*pipe.fail && !mbar_wait(&pipe.full[st], (uint32_t)((t / kStages) & 1))) *pipe.fail = 1;
+      score_tile_mma<D, G, TR>(ring_a + st * kStageBytes, 16 * sub, min(TR, N - t * TR), t * TR, scores, ss, w);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pipe.empty[st]);
+    }
+  }
+  __syncthreads();
+  if (*pipe.fail) {
+    if (tid == 0) {
+      const int issued = *pipe.issued;
+      for (int st = 0; st < kStages && st < issued; ++st) {
+        const int last = st + ((issued - 1 - st) / kStages) * kStages;
+        mbar_wait(&pipe.full[st], (uint32_t)((last / kStages) & 1));
+      }
+    }
+    return;
+  }
+
+  float mu[G], inv[G];
+  head_moments<G>(scores, ss, N, red, mu, inv);
+  uint32_t *keys = reinterpret_cast<uint32_t *>(scores);   // overlays head 0's scores
+  for (int i = tid; i < N; i += nt) {
+    float sv[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) sv[h] = scores[h * ss + i];
+    float z = (sv[0] - mu[0]) * inv[0];
+#pragma unroll
+    for (int h = 1; h < G; ++h) z = fmaxf(z, (sv[h] - mu[h]) * inv[h]);
+    if (a.mode == 1) {
+      a.agg[(long long)u * c.cap + i] = z;
+      if (a.raw != nullptr) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * c.cap + i] = sv[h];
+      }
+    } else {
+      keys[i] = score_key(z);
+    }
+  }
+  if (a.mode == 1) return;
+  __syncthreads();
+  int ntie;
+  const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
+  const int e0 = build_kept_chunked(keys, N, B, T, ntie, idxs, sm);
+  if (a.holefill) {
+    holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), sm,
+                  a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
+    return;
+  }
+  if (a.idx_out != nullptr)
+    for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
+  // The ring was last read by ldmatrix (generic proxy); TMA writes it next.
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (warp == 0) compact_unit_runs(c, l, s, g, idxs, e0, B, N, ring, cbars);
 }
 
 // Chan's combination of (count, mean, M2) summaries: (n, mean, M2) absorbs (nb, mb, Mb).
@@ -1036,6 +1184,19 @@ static tri_status set_smem(K kernel, int bytes) {
 template <int D, int G, bool BF16>
 static tri_status run_fused(const FusedArgs &a, int64_t units, cudaStream_t st) {
   const FusedLayout lay(G, D / 2, a.capp);
+  if constexpr (BF16) {
+    if (a.mma_ok) {
+      FusedMmaArgs m;
+      std::memset(&m, 0, sizeof(m));
+      m.f = a;
+      if (make_swizzled_map(a.cache, a.params, &m.ks)) {
+        auto k = fused_mma_kernel<D, G>;
+        if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
+        k<<<(unsigned)units, kThreads, lay.total, st>>>(m);
+        return launch_result();
+      }
+    }
+  }
   auto k = fused_kernel<D, G, BF16>;
   if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
   k<<<(unsigned)units, kFusedThreads, lay.total, st>>>(a);
@@ -1105,6 +1266,9 @@ static FusedArgs fused_args(const tri_cache *c, const tri_stats *stt, const tri_
   a.inter = p->pairing == TRI_PAIR_INTERLEAVED;
   a.capp = round32(c->cap);
   a.sc = make_const(p, c->d);
+  a.mma_ok = kFusedMma;
+  a.cache = c;
+  a.params = p;
   return a;
 }
 

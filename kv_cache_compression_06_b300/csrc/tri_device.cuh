@@ -13,6 +13,10 @@
 namespace tri {
 
 constexpr int kFusedThreads = 256;             // CTA size of the fused short-unit kernel
+#ifndef TRI_FUSED_MMA
+#define TRI_FUSED_MMA 1
+#endif
+constexpr int kFusedMma = TRI_FUSED_MMA;       // short units of bf16 rotate-half caches on the tensor cores
 constexpr int kConsumerWarps = 8;              // warps that score keys (long-unit tiles)
 constexpr int kProducerWarp = kConsumerWarps;   // the warp that issues the K loads
 constexpr int kThreads = (kConsumerWarps + 1) * 32;   // CTA size of the long-unit score kernel
