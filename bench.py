@@ -344,8 +344,12 @@ def run_b300(args, w):
         return
     peak, peak_kind = _peaks()
     achieved = alg_bytes / t_step / 1e9
-    kname = (f"fused_kernel<{w.d},{w.G},{w.dtype}>" if launches == 1
-             else "phase_kernel+score_tiles_mma_kernel+select_compact_kernel")
+    mma = w.dtype == "bf16" and w.pairing == "half"
+    if launches == 1:
+        kname = f"fused_mma_kernel<{w.d},{w.G}>" if mma else f"fused_kernel<{w.d},{w.G},{w.dtype}>"
+    else:
+        kname = ("phase_kernel+" + ("score_tiles_mma_kernel" if mma else "score_tiles_kernel")
+                 + "+select_compact_kernel")
     line = {
         "metric": METRIC, "value": job_throughput(world, n_keys, t_step), "unit": "keys/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
