@@ -53,14 +53,22 @@ def _config(w, extra=None):
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def oracle_sample(w, budget_s, max_units=None, seed=0):
-    """Runs the fp64 oracle on sampled units of layer 0 (generated on the CPU)
-    until budget_s seconds of CPU work; returns (keys, seconds, units, threads)."""
+def oracle_layer(w):
+    """Layer 0 of the workload on the CPU with the oracle's statistics (untimed)."""
     from oracle import tri_oracle as O
     from synth import generate_layer
 
     lay = generate_layer(w, 0, "cpu", with_q=True)
-    stats = O.calibrate(lay["q_pre"].double().numpy(), w.pairing)
+    return lay, O.calibrate(lay["q_pre"].double().numpy(), w.pairing)
+
+
+def oracle_sample(w, budget_s, max_units=None, seed=0, layer=None):
+    """Runs the fp64 oracle on sampled units of layer 0 (generated on the CPU,
+    or the given oracle_layer) until budget_s seconds of CPU work; returns
+    (keys, seconds, units, threads)."""
+    from oracle import tri_oracle as O
+
+    lay, stats = layer if layer is not None else oracle_layer(w)
     rng = np.random.default_rng(seed)
     keys = units = 0
     t0 = time.perf_counter()
@@ -85,8 +93,9 @@ def run_reference(args, w):
         return
     per_step = []
     total_keys = 0
+    layer = oracle_layer(w)
     for i in range(args.warmup + args.steps):
-        keys, el, units, cores = oracle_sample(w, 0.0, max_units=2, seed=1000 + i)
+        keys, el, units, cores = oracle_sample(w, 0.0, max_units=2, seed=1000 + i, layer=layer)
         if i >= args.warmup:
             per_step.append(el)
             total_keys += keys
