@@ -377,8 +377,10 @@ __device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUten
   if (lane < nblk) {
     const int b = c.bt[(long long)s * c.max_blocks + row0 / blk + lane];
     const int z = (int)((long long)l * c.nblocks + b);
-#pragma unroll
-    for (int hh = 0; hh < NH; ++hh) tma_load_4d(dst + hh * TR * 128 + lane * blk * 128, map, 64 * hh, g, 0, z, full);
+    if constexpr (NH == 2)
+      tma_load_5d(dst + lane * blk * 256, map, 0, 0, 0, g, z, full);   // [half][blk rows] of one block
+    else
+      tma_load_4d(dst + lane * blk * 128, map, 0, g, 0, z, full);
   }
 }
 
@@ -495,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
         const int st = t % kStages;
         if (!*pipe.fail && !mbar_wait(&pipe.full[st], (uint32_t)((t / kStages) & 1))) *pipe.fail = 1;
         score_tile_mma<D, G, TR>(ring + st * kStageBytes, 16 * sub, min(TR, n - t * TR), (t - tbeg) * TR,
-                                 scores, TS, w);
+                                 scores, TS, w, c.paged() ? c.block : 0);
         __syncwarp();
         if (lane == 0) mbar_arrive(&pipe.empty[st]);
       }
@@ -621,7 +623,8 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
     for (int t = grp; t < nst; t += GROUPS) {
       const int st = t % kStages;
       if (!*pipe.fail && !mbar_wait(&pipe.full[st], (uint32_t)((t / kStages) & 1))) *pipe.fail = 1;
-      score_tile_mma<D, G, TR>(ring_a + st * kStageBytes, 16 * sub, min(TR, N - t * TR), t * TR, scores, ss, w);
+      score_tile_mma<D, G, TR>(ring_a + st * kStageBytes, 16 * sub, min(TR, N - t * TR), t * TR, scores, ss, w,
+                               c.paged() ? c.block : 0);
       __syncwarp();
       if (lane == 0) mbar_arrive(&pipe.empty[st]);
     }
@@ -1097,6 +1100,20 @@ static bool make_swizzled_map(const tri_cache *c, const tri_params *p, CUtensorM
     const cuuint32_t box[2] = {64u, (cuuint32_t)tr};
     const cuuint32_t estr[2] = {1u, 1u};
     r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->k, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (c->d == 128) {
+    // 5-D view (64 elements, block rows, halves, heads, blocks) with a box of
+    // one block of one head, both halves: smem [half][block rows][128 B]
+    if (c->block > 256 || c->block % 8 != 0 || tr % c->block != 0 || tr / c->block > 32) return false;
+    if ((int64_t)c->L * c->nblocks >= (1ll << 31)) return false;
+    const cuuint64_t dims[5] = {64u, (cuuint64_t)c->block, 2u, (cuuint64_t)c->Hkv,
+                                (cuuint64_t)c->L * (cuuint64_t)c->nblocks};
+    const cuuint64_t strides[4] = {(cuuint64_t)c->Hkv * rb, 128u, (cuuint64_t)rb,
+                                   (cuuint64_t)c->block * c->Hkv * rb};
+    const cuuint32_t box[5] = {64u, (cuuint32_t)c->block, 2u, 1u, 1u};
+    const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, c->k, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {

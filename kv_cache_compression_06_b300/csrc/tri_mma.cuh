@@ -19,7 +19,9 @@
 // K arrives in shared memory through 128B-swizzled tensor copies: a stage is
 // [half][TR rows][128 B] (d = 128: half 0 = Re (elements 0..63), half 1 = Im;
 // d = 64: one half holding both), the 16-byte chunk c of row r stored at chunk
-// c ^ (r & 7), which makes the ldmatrix row reads conflict-free.
+// c ^ (r & 7), which makes the ldmatrix row reads conflict-free.  A paged
+// d = 128 stage is one such [half][blk rows][128 B] group per cache block (one
+// tensor copy per block carries both halves).
 #pragma once
 
 #include "tri_path.cuh"
@@ -118,28 +120,48 @@ __device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, const floa
   }
 }
 
-// Shared-memory byte address of element column `col` (a multiple of 8) of row
-// `row` in a swizzled stage of TR rows.
+// Position of one row in a swizzled stage: byte offset of its 128-byte segment
+// in half 0, the stride between halves, and its swizzle key.  blk = 0: the
+// stage is [half][TR rows]; blk > 0 (paged, d = 128): [block][half][blk rows].
+struct SwRow {
+  int off, hstride, key;
+};
 template <int TR>
-__device__ __forceinline__ uint32_t sw_addr(uint32_t stage, int row, int col) {
-  return stage + (uint32_t)((col >> 6) * (TR * 128) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
+__device__ __forceinline__ SwRow sw_row(int row, int blk) {
+  SwRow r;
+  if (blk > 0) {
+    const int b = row / blk, rr = row - b * blk;
+    r.off = b * blk * 256 + rr * 128;
+    r.hstride = blk * 128;
+    r.key = rr & 7;
+  } else {
+    r.off = row * 128;
+    r.hstride = TR * 128;
+    r.key = row & 7;
+  }
+  return r;
+}
+// Byte address of element column `col` (a multiple of 8) of that row.
+__device__ __forceinline__ uint32_t sw_addr(uint32_t stage, const SwRow &r, int col) {
+  return stage + (uint32_t)(r.off + (col >> 6) * r.hstride + ((((col & 63) >> 3) ^ r.key) << 4));
 }
 
 // Scores the 16 keys at stage rows [r0, r0 + 16) (row0 + r0 + i is the key's
 // index in the caller's score rows); rows at or past nrows are not stored.
 template <int D, int G, int TR>
 __device__ __forceinline__ void score_tile_mma(uint32_t stage, int r0, int nrows, int row0, float *scores,
-                                               int sstride, const MmaWeights<D, G> &w) {
+                                               int sstride, const MmaWeights<D, G> &w, int blk) {
   constexpr int F = D / 2;
   const int lane = threadIdx.x & 31;
   const int lrow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row of this lane
   const int lcol = (lane >> 4) * 8;                           // and column offset
+  const SwRow sr = sw_row<TR>(lrow, D == 128 ? blk : 0);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int ks = 0; ks < F / 16; ++ks) {
     uint32_t re[4], im[4];
-    ldmatrix_x4(re[0], re[1], re[2], re[3], sw_addr<TR>(stage, lrow, 16 * ks + lcol));
-    ldmatrix_x4(im[0], im[1], im[2], im[3], sw_addr<TR>(stage, lrow, F + 16 * ks + lcol));
+    ldmatrix_x4(re[0], re[1], re[2], re[3], sw_addr(stage, sr, 16 * ks + lcol));
+    ldmatrix_x4(im[0], im[1], im[2], im[3], sw_addr(stage, sr, F + 16 * ks + lcol));
     mma_bf16(acc, re, w.bt[ks][0], w.bt[ks][1]);
     mma_bf16(acc, im, w.bt[F / 16 + ks][0], w.bt[F / 16 + ks][1]);
     if constexpr (G == 8) {
