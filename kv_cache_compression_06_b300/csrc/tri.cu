@@ -18,6 +18,7 @@
 //                        (from agg) and tri_compact_kv (from idx).
 #include <cmath>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -773,6 +774,7 @@ struct SCArgs {
   const float *agg;
   const int *idx_in;
   int *idx_out, *new_len;
+  uint32_t *keys;   // select2_kernel: workspace [units][capp] (16-byte aligned rows)
 };
 
 // The keys (one u32 per slot) and the compaction ring share one region at the
@@ -957,6 +959,93 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
       compact_unit_tma(c, &a.maps, tid >> 5, l, s, g, idxs, e0, B, N, ring, lay.nstages,
                        cbars + (tid >> 5) * kMaxCompactStages);
   }
+}
+
+// ---------------------------------------------------------------- long units: select/compact, two per SM
+// The compress step's long-unit select/compact (select_compact_kernel mode 0)
+// with its keys in the workspace instead of shared memory: 256 threads, a
+// 6-stage compaction ring, ~106 KB of shared memory, so two CTAs (units) share
+// an SM and one unit's selection overlaps the other's compaction traffic.
+constexpr int kSel2Threads = 256;
+constexpr int kSel2Stages = 6;
+
+struct Sel2Layout {
+  int bars, hist, sm, mom, idx, total;
+  __host__ __device__ explicit Sel2Layout(int bcap) {
+    int o = kSel2Stages * kStageBytes;   // ring (also the hole-fill bookkeeping)
+    bars = o; o += 2 * kSel2Stages * 8;
+    hist = o; o += 1024;
+    sm = o;   o += kSelInts * 4;
+    mom = o;  o += 128;
+    idx = o;  o += align_up(bcap * 4, 128);
+    total = o;
+  }
+};
+
+__global__ void __launch_bounds__(kSel2Threads, 2) select2_kernel(const __grid_constant__ SCArgs a) {
+  extern __shared__ __align__(1024) char smem[];
+  const Sel2Layout lay(a.bcap);
+  char *ring = smem;
+  uint64_t *cbars = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  uint32_t *hist = reinterpret_cast<uint32_t *>(smem + lay.hist);
+  int *sm = reinterpret_cast<int *>(smem + lay.sm);
+  float *mom = reinterpret_cast<float *>(smem + lay.mom);
+  int *idxs = reinterpret_cast<int *>(smem + lay.idx);
+  const CacheView &c = a.c;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int u = blockIdx.x;
+  const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
+  if (timed_out()) return;
+  const int N = c.seq_len[s];
+  const int B = a.budget;
+  if (N < 0 || N > c.cap) {
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  const bool len_writer = tid == 0 && a.new_len != nullptr && l == 0 && g == 0;
+  if (N <= B) {
+    if (len_writer) a.new_len[s] = N;
+    if (a.idx_out != nullptr)
+      for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = j < N ? j : -1;
+    return;
+  }
+  if (!c.blocks_ok(s, N)) {   // the sequence is skipped: its length stays N
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    if (len_writer) a.new_len[s] = N;
+    return;
+  }
+  if (len_writer) a.new_len[s] = B;
+  if (tid == 0) {
+    for (int st = 0; st < kSel2Stages; ++st) {
+      mbar_init(&cbars[st], 1);                  // K warp
+      mbar_init(&cbars[kSel2Stages + st], 1);    // V warp
+    }
+    fence_mbar_init();
+  }
+  merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom);
+  __syncthreads();
+  uint32_t *keys = a.keys + (long long)u * a.capp;
+  const float *raw_u = a.raw + (long long)u * a.G * a.capp;
+  switch (a.G) {
+    case 1: zmax_from_raw<1>(raw_u, a.capp, N, mom, keys); break;
+    case 2: zmax_from_raw<2>(raw_u, a.capp, N, mom, keys); break;
+    case 4: zmax_from_raw<4>(raw_u, a.capp, N, mom, keys); break;
+    default: zmax_from_raw<8>(raw_u, a.capp, N, mom, keys); break;
+  }
+  __syncthreads();   // the keys (global) are visible to the whole CTA
+  int ntie;
+  const uint32_t T = radix_select_gmem(keys, N, B, hist, sm, &ntie);
+  const int e0 = build_kept_gmem(keys, N, B, T, ntie, idxs, sm);
+  if (a.holefill) {
+    holefill_unit(c, l, s, g, idxs, B, N, ring, sm, a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
+    return;
+  }
+  if (a.idx_out != nullptr)
+    for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
+  __syncthreads();
+  if ((tid >> 5) < 2)
+    compact_unit_tma(c, &a.maps, tid >> 5, l, s, g, idxs, e0, B, N, ring, kSel2Stages,
+                     cbars + (tid >> 5) * kSel2Stages);
 }
 
 // ================================================================ host side
@@ -1166,7 +1255,7 @@ static bool fused_fits(const tri_cache *c, int G) {
 }
 
 struct SplitWs {
-  size_t raw_off, part_off, phase_off, total;
+  size_t raw_off, part_off, phase_off, keys_off, total;
 };
 static SplitWs split_ws(const tri_cache *c, int G) {
   SplitWs w;
@@ -1176,8 +1265,10 @@ static SplitWs split_ws(const tri_cache *c, int G) {
   const size_t phase = (size_t)c->S * (c->d / 2) * sizeof(float2);
   w.raw_off = 0;
   w.part_off = (raw + 255) / 256 * 256;
+  const size_t keys = (size_t)units_of(c) * (size_t)round32(c->cap) * sizeof(uint32_t);
   w.phase_off = w.part_off + (part + 255) / 256 * 256;
-  w.total = w.phase_off + (phase + 255) / 256 * 256;
+  w.keys_off = w.phase_off + (phase + 255) / 256 * 256;
+  w.total = w.keys_off + (keys + 255) / 256 * 256;
   return w;
 }
 
@@ -1513,6 +1604,17 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   sa.part = ta.part;
   sa.idx_out = idx_out;
   sa.new_len = new_len;
+  sa.keys = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + w.keys_off);
+  // two units per SM when the hole-fill bookkeeping (B bytes + 4 min(B, N - B))
+  // fits the smaller ring; else the one-per-SM kernel with keys in shared memory
+  const Sel2Layout l2(sa.bcap);
+  const int64_t movers = std::min<int64_t>(params->budget, cache->cap - params->budget);
+  const bool hf_fits = !sa.holefill || params->budget + 16 + 4 * std::max<int64_t>(movers, 0) <= kSel2Stages * kStageBytes;
+  if (l2.total <= kMaxSmem && hf_fits) {
+    if (set_smem(select2_kernel, l2.total) != TRI_OK) return TRI_ERR_CUDA;
+    select2_kernel<<<(unsigned)units, kSel2Threads, l2.total, stream>>>(sa);
+    return launch_result();
+  }
   return run_select_compact(sa, units, stream);
 }
 

@@ -642,6 +642,131 @@ __device__ __noinline__ int build_kept(const uint32_t *keys, int n, int K, uint3
   return e0;
 }
 
+// ---------------------------------------------------------------- top-B over keys in global memory
+// Variants of radix_select_atomic / build_kept for keys stored in global memory
+// (L2-resident: one unit's keys are 4 N bytes), used by the long-unit select
+// kernel so that its shared memory fits two CTAs per SM.  Rows of keys are
+// 16-byte aligned; the reads are 16-byte vectors (radix) or 8 steps of 32
+// consecutive keys per warp issued together (kept list).
+
+// Radix select as radix_select_atomic, reading keys4[0..ceil(n/4)).
+__device__ __noinline__ uint32_t radix_select_gmem(const uint32_t *keys, int n, int K, uint32_t *hist, int *sm,
+                                                   int *ntie) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+  const uint4 *keys4 = reinterpret_cast<const uint4 *>(keys);
+  const int n4 = (n + 3) / 4;
+  uint32_t prefix = 0, mask = 0;
+  int k = K;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += nt) hist[b] = 0;
+    __syncthreads();
+#pragma unroll 4
+    for (int q = tid; q < n4; q += nt) {
+      const uint4 v = keys4[q];
+      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (4 * q + j < n && (e[j] & mask) == prefix) atomicAdd(&hist[(e[j] >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    int P = 0, wsum = 0;
+    if (tid < 256) {
+      P = (int)hist[255 - tid];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, P, o);
+        if (lane >= o) P += y;
+      }
+      if (lane == 31) sm[8 + warp] = P;
+    }
+    __syncthreads();
+    if (tid < 256) {
+      for (int w = 0; w < warp; ++w) wsum += sm[8 + w];
+      P += wsum;
+      int Pprev = __shfl_up_sync(0xffffffffu, P, 1);
+      if (lane == 0) Pprev = wsum;
+      if (P >= k && Pprev < k) {
+        sm[0] = 255 - tid;
+        sm[1] = k - Pprev;
+      }
+    }
+    __syncthreads();
+    const uint32_t dgt = (uint32_t)sm[0];
+    k = sm[1];
+    prefix |= dgt << shift;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  *ntie = k;
+  return prefix;
+}
+
+// build_kept over keys in global memory (same result and shared scratch).
+__device__ __noinline__ int build_kept_gmem(const uint32_t *keys, int n, int K, uint32_t T, int ntie, int *idx,
+                                            int *sm) {
+  constexpr int PF = 8;   // steps of 32 keys loaded together
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int seg = (((n + nw - 1) / nw) + 31) / 32 * 32;
+  const int lo = min(n, warp * seg), hi = min(n, lo + seg);
+  int cgt = 0, ceq = 0;
+  for (int base = lo; base < hi; base += 32 * PF) {
+    uint32_t u[PF];
+#pragma unroll
+    for (int e = 0; e < PF; ++e) {
+      const int i = base + 32 * e + lane;
+      u[e] = i < hi ? keys[i] : 0u;
+    }
+#pragma unroll
+    for (int e = 0; e < PF; ++e) {
+      const bool in = base + 32 * e + lane < hi;
+      cgt += __popc(__ballot_sync(0xffffffffu, in && u[e] > T));
+      ceq += __popc(__ballot_sync(0xffffffffu, in && u[e] == T));
+    }
+  }
+  if (lane == 0) {
+    sm[24 + warp] = ceq;
+    sm[40 + warp] = cgt;
+  }
+  if (tid == 0) sm[56] = n;
+  __syncthreads();
+  int eq_before = 0, kept_before = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int e = sm[24 + w];
+    const int tw = max(0, min(e, ntie - eq_before));
+    kept_before += sm[40 + w] + tw;
+    eq_before += e;
+  }
+  const unsigned lt = lanemask_lt();
+  int eq_run = eq_before, pos_run = kept_before, first_drop = n;
+  for (int base = lo; base < hi; base += 32 * PF) {
+    uint32_t u[PF];
+#pragma unroll
+    for (int e = 0; e < PF; ++e) {
+      const int i = base + 32 * e + lane;
+      u[e] = i < hi ? keys[i] : 0u;
+    }
+#pragma unroll
+    for (int e = 0; e < PF; ++e) {
+      const int i = base + 32 * e + lane;
+      const bool valid = i < hi;
+      const unsigned eqm = __ballot_sync(0xffffffffu, valid && u[e] == T);
+      const bool keep = valid && (u[e] > T || (u[e] == T && eq_run + __popc(eqm & lt) < ntie));
+      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      const unsigned dm = __ballot_sync(0xffffffffu, valid && !keep);
+      const int pos = pos_run + __popc(km & lt);
+      if (keep && pos < K) idx[pos] = i;
+      if (dm != 0u && first_drop == n) first_drop = base + 32 * e + __ffs(dm) - 1;
+      eq_run += __popc(eqm);
+      pos_run += __popc(km);
+    }
+  }
+  if (lane == 0 && first_drop < n) atomicMin(&sm[56], first_drop);
+  __syncthreads();
+  const int e0 = sm[56];
+  __syncthreads();
+  return e0;
+}
+
 // ---------------------------------------------------------------- compaction (a5)
 // Short-unit variant of the compaction (the fused kernel's): warp 0 alone, bulk
 // copies only, a fixed ring of kStages stages.  Its per-chunk issue path is the
