@@ -385,30 +385,57 @@ __device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUten
   }
 }
 
-// Mean and M2 per head over one tile's scores by the consumer warps only
-// (named barrier 1), shifted by the tile's first score as head_mean_m2.
+// Writes one tile's raw scores (G rows of tn floats, head h at raw + h *
+// rstride) and returns their (mean, M2) per head, taken on the scores minus the
+// tile's first score (a constant head gets M2 = 0 exactly); one pass stores and sums, a second
+// sums the squared deviations.  vec: 16-byte loads and stores (raw rows
+// 16-byte aligned); else 4-byte ones.
 template <int G>
-__device__ __forceinline__ void tile_mean_m2(const float *scores, int stride, int n, float *red, int nthreads,
-                                             float (&mu)[G], float (&m2)[G]) {
+__device__ __forceinline__ void tile_flush(const float *scores, int stride, int tn, float *raw, long long rstride,
+                                           bool vec, float *red, int nthreads, float (&mu)[G], float (&m2)[G]) {
+  const int tid = threadIdx.x;
   float v[G], sh[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     v[h] = 0.f;
     sh[h] = scores[h * stride];
   }
-  for (int i = threadIdx.x; i < n; i += nthreads) {
+  const int n4 = vec ? tn >> 2 : 0;
+  for (int q = tid; q < n4; q += nthreads) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) v[h] += scores[h * stride + i] - sh[h];
+    for (int h = 0; h < G; ++h) {
+      const float4 x = reinterpret_cast<const float4 *>(scores + h * stride)[q];
+      reinterpret_cast<float4 *>(raw + h * rstride)[q] = x;
+      v[h] += ((x.x - sh[h]) + (x.y - sh[h])) + ((x.z - sh[h]) + (x.w - sh[h]));
+    }
+  }
+  for (int i = 4 * n4 + tid; i < tn; i += nthreads) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float x = scores[h * stride + i];
+      raw[h * rstride + i] = x;
+      v[h] += x - sh[h];
+    }
   }
   group_sum<G>(v, red, nthreads);
   float md[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    md[h] = v[h] / (float)n;
+    md[h] = v[h] / (float)tn;
     mu[h] = sh[h] + md[h];
     v[h] = 0.f;
   }
-  for (int i = threadIdx.x; i < n; i += nthreads) {
+  const int m4 = tn >> 2;
+  for (int q = tid; q < m4; q += nthreads) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float4 x = reinterpret_cast<const float4 *>(scores + h * stride)[q];
+      const float d0 = (x.x - sh[h]) - md[h], d1 = (x.y - sh[h]) - md[h];
+      const float d2 = (x.z - sh[h]) - md[h], d3 = (x.w - sh[h]) - md[h];
+      v[h] = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, v[h]))));
+    }
+  }
+  for (int i = 4 * m4 + tid; i < tn; i += nthreads) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float dl = (scores[h * stride + i] - sh[h]) - md[h];
@@ -489,9 +516,11 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
     if (lane == 0) *pipe.issued = t;
   } else {
     MmaWeights<D, G> w;
-    load_mma_weights<D, G>(w, wts);
+    load_mma_weights<D, G>(w, wts, kConsumerWarps * 32, warp == 0);
     const int grp = warp / SPS, sub = warp % SPS;
     const uint32_t ring = smem_u32(pipe.ring);
+    // tiles start at multiples of 64 keys: 16-byte raw stores when the rows are aligned
+    const bool raw_vec = (a.raw_stride & 3) == 0 && (reinterpret_cast<uintptr_t>(a.raw) & 15) == 0;
     for (int tt = 0; tt * SPT < nst; ++tt) {   // tiles of this CTA
       const int tbeg = tt * SPT, tend = min(nst, tbeg + SPT);
       for (int t = tbeg + (grp - tbeg % GROUPS + GROUPS) % GROUPS; t < tend; t += GROUPS) {
@@ -506,12 +535,9 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
       const int tn = min(TK, n - tbeg * TR);
       const int ti0 = i0 + tbeg * TR;
       if (!*pipe.fail) {
-        for (int i = tid; i < tn; i += NC) {
-#pragma unroll
-          for (int h = 0; h < G; ++h) a.raw[((long long)u * G + h) * a.raw_stride + ti0 + i] = scores[h * TS + i];
-        }
         float mu[G], m2[G];
-        tile_mean_m2<G>(scores, TS, tn, red, NC, mu, m2);
+        tile_flush<G>(scores, TS, tn, a.raw + (long long)u * G * a.raw_stride + ti0, a.raw_stride, raw_vec, red, NC,
+                      mu, m2);
         if (tid == 0) {
 #pragma unroll
           for (int h = 0; h < G; ++h)
@@ -618,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
     if (lane == 0) *pipe.issued = t;
   } else {
     MmaWeights<D, G> w;
-    load_mma_weights<D, G>(w, wts);
+    load_mma_weights<D, G>(w, wts, kConsumerWarps * 32, warp == 0);
     const int grp = warp / SPS, sub = warp % SPS;
     const uint32_t ring_a = smem_u32(ring);
     for (int t = grp; t < nst; t += GROUPS) {

@@ -60,18 +60,28 @@ __device__ __forceinline__ void split_bf16x2(float v0, float v1, uint32_t &hi, u
 // B fragments (weights) of one warp, for D / 16 trig k-steps (Re then Im
 // blocks of 16 bands) and F / 16 magnitude k-steps.
 //   G <= 4: bt[ks] = [hi | lo] columns; bm[ks] = [hi | lo]; bm2[ks] = [hi | 0]
-//   G == 8: bt/bm = hi, bt2/bm2 = lo
+//   G == 8: bt/bm = hi; the lo fragments stay in shared memory ([KT + KM][32
+//           lanes] pairs at `lo`: trig k-steps, then magnitude k-steps; `lo`
+//           addresses this lane's pair of k-step 0), read back per k-step,
+//           which keeps the kernel within 96 registers
 template <int D, int G>
 struct MmaWeights {
   static constexpr int KT = D / 16, KM = D / 32;
-  uint32_t bt[KT][2], bm[KM][2], bm2[KM][2];
-  uint32_t bt2[G == 8 ? KT : 1][2];
+  uint32_t bt[KT][2], bm[KM][2], bm2[G == 8 ? 1 : KM][2];
+  uint32_t lo;
 };
+
+__device__ __forceinline__ void lds_v2(uint32_t (&r)[2], uint32_t addr) {
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
 
 // Builds this lane's B fragments from wts [G][3][F] (Re A, Im A, W).  Lane l
 // holds column n = l / 4 and rows k = 2 (l % 4) + {0, 1, 8, 9} of each k-step.
+// Called by all nc consumer threads (named barrier 1); for G == 8 the first
+// consumer warp (`writer`) then overwrites the start of wts with the lo trig
+// fragments (wts is dead once every consumer holds its fragments).
 template <int D, int G>
-__device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, const float *wts) {
+__device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, float *wts, int nc, bool writer) {
   constexpr int F = D / 2;
   const int lane = threadIdx.x & 31, n = lane >> 2, k0 = 2 * (lane & 3);
   const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
@@ -79,6 +89,7 @@ __device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, const floa
   const int h = G == 8 ? n : (n & 3);
   const bool live = G == 8 || h < G;
   const int part = G == 8 ? 0 : (n >> 2);
+  uint32_t lo[G == 8 ? MmaWeights<D, G>::KT + MmaWeights<D, G>::KM : 1][2];
 #pragma unroll
   for (int ks = 0; ks < MmaWeights<D, G>::KT; ++ks) {
     // features 16 ks + k: Re A for bands < F, Im A after
@@ -94,8 +105,8 @@ __device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, const floa
     w.bt[ks][0] = part ? l01 : h01;
     w.bt[ks][1] = part ? l23 : h23;
     if constexpr (G == 8) {
-      w.bt2[ks][0] = l01;
-      w.bt2[ks][1] = l23;
+      lo[ks][0] = l01;
+      lo[ks][1] = l23;
     }
   }
 #pragma unroll
@@ -109,14 +120,26 @@ __device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, const floa
     if constexpr (G == 8) {
       w.bm[ks][0] = h01;
       w.bm[ks][1] = h23;
-      w.bm2[ks][0] = l01;
-      w.bm2[ks][1] = l23;
+      lo[MmaWeights<D, G>::KT + ks][0] = l01;
+      lo[MmaWeights<D, G>::KT + ks][1] = l23;
     } else {
       w.bm[ks][0] = part ? l01 : h01;
       w.bm[ks][1] = part ? l23 : h23;
       w.bm2[ks][0] = part ? 0u : h01;
       w.bm2[ks][1] = part ? 0u : h23;
     }
+  }
+  w.lo = 0;
+  if constexpr (G == 8) {
+    uint2 *dst = reinterpret_cast<uint2 *>(wts);
+    named_sync(1, nc);   // every consumer has read wts
+    if (writer) {
+#pragma unroll
+      for (int ks = 0; ks < MmaWeights<D, G>::KT + MmaWeights<D, G>::KM; ++ks)
+        dst[ks * 32 + lane] = make_uint2(lo[ks][0], lo[ks][1]);
+    }
+    named_sync(1, nc);
+    w.lo = smem_u32(dst) + lane * 8;
   }
 }
 
@@ -156,7 +179,8 @@ __device__ __forceinline__ void score_tile_mma(uint32_t stage, int r0, int nrows
   const int lrow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row of this lane
   const int lcol = (lane >> 4) * 8;                           // and column offset
   const SwRow sr = sw_row<TR>(lrow, D == 128 ? blk : 0);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // two accumulators (trig, magnitude): two shorter dependent MMA chains
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int ks = 0; ks < F / 16; ++ks) {
     uint32_t re[4], im[4];
@@ -165,8 +189,11 @@ __device__ __forceinline__ void score_tile_mma(uint32_t stage, int r0, int nrows
     mma_bf16(acc, re, w.bt[ks][0], w.bt[ks][1]);
     mma_bf16(acc, im, w.bt[F / 16 + ks][0], w.bt[F / 16 + ks][1]);
     if constexpr (G == 8) {
-      mma_bf16(acc, re, w.bt2[ks][0], w.bt2[ks][1]);
-      mma_bf16(acc, im, w.bt2[F / 16 + ks][0], w.bt2[F / 16 + ks][1]);
+      uint32_t lr[2], li[2];
+      lds_v2(lr, w.lo + ks * 256);
+      lds_v2(li, w.lo + (F / 16 + ks) * 256);
+      mma_bf16(acc, re, lr[0], lr[1]);
+      mma_bf16(acc, im, li[0], li[1]);
     }
     // |k~| at the same fragment positions, split into hi + lo
     uint32_t mh[4], ml[4];
@@ -178,14 +205,18 @@ __device__ __forceinline__ void score_tile_mma(uint32_t stage, int r0, int nrows
           a, b);
       split_bf16x2(sqrt_approx(a), sqrt_approx(b), mh[e], ml[e]);
     }
-    mma_bf16(acc, mh, w.bm[ks][0], w.bm[ks][1]);
+    mma_bf16(accm, mh, w.bm[ks][0], w.bm[ks][1]);
     if constexpr (G == 8) {
-      mma_bf16(acc, mh, w.bm2[ks][0], w.bm2[ks][1]);   // hi x lo
-      mma_bf16(acc, ml, w.bm[ks][0], w.bm[ks][1]);     // lo x hi
+      uint32_t lm[2];
+      lds_v2(lm, w.lo + (D / 16 + ks) * 256);
+      mma_bf16(accm, mh, lm[0], lm[1]);                 // hi x lo
+      mma_bf16(accm, ml, w.bm[ks][0], w.bm[ks][1]);     // lo x hi
     } else {
-      mma_bf16(acc, ml, w.bm2[ks][0], w.bm2[ks][1]);   // lo x hi (lo columns get 0)
+      mma_bf16(accm, ml, w.bm2[ks][0], w.bm2[ks][1]);   // lo x hi (lo columns get 0)
     }
   }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) acc[e] += accm[e];
   // D fragment: acc[0..1] row r, columns n, n + 1; acc[2..3] row r + 8.
   const int r = lane >> 2, n = 2 * (lane & 3);
   if constexpr (G == 8) {
