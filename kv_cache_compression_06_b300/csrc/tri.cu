@@ -895,7 +895,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
   uint32_t *keys = reinterpret_cast<uint32_t *>(smem + lay.keys);
   int *idxs = reinterpret_cast<int *>(smem + lay.idx);
   const CacheView &c = a.c;
-  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
+  const int tid = threadIdx.x, nt = blockDim.x;
   const int u = blockIdx.x;
   const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
   if (timed_out()) return;
