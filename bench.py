@@ -179,6 +179,18 @@ def _traffic_record(kernel_src_hash, workload, layers):
     return None
 
 
+def _select_kernel_name(w, cap, compact):
+    """The long-unit select/compact kernel tri_compress_step launches: the
+    two-per-SM select2_kernel when its shared memory holds the kept list and,
+    for hole-fill, the hole bookkeeping (B + 16 + 4 min(B, cap - B) bytes in a
+    6 x 16 KB ring); else select_compact_kernel."""
+    B = w.budget
+    bcap = -(-min(B, cap) // 32) * 32
+    total = 6 * 16384 + 96 + 1024 + 256 + 128 + -(-bcap * 4 // 128) * 128
+    hf_ok = compact != "holefill" or B + 16 + 4 * max(min(B, cap - B), 0) <= 6 * 16384
+    return "select2_kernel" if total <= 232448 and hf_ok else "select_compact_kernel"
+
+
 def kernel_src_hash():
     import hashlib
     h = hashlib.sha1()
@@ -358,7 +370,7 @@ def run_b300(args, w):
         kname = f"fused_mma_kernel<{w.d},{w.G}>" if mma else f"fused_kernel<{w.d},{w.G},{w.dtype}>"
     else:
         kname = ("phase_kernel+" + ("score_tiles_mma_kernel" if mma else "score_tiles_kernel")
-                 + "+select_compact_kernel")
+                 + "+" + _select_kernel_name(w, cache.cap, args.compact))
     line = {
         "metric": METRIC, "value": job_throughput(world, n_keys, t_step), "unit": "keys/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
