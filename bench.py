@@ -181,13 +181,13 @@ def _traffic_record(kernel_src_hash, workload, layers):
 
 def _select_kernel_name(w, cap, compact):
     """The long-unit select/compact kernel tri_compress_step launches: the
-    two-per-SM select2_kernel when its shared memory holds the kept list and,
+    three-per-SM select2_kernel when its shared memory holds the kept list and,
     for hole-fill, the hole bookkeeping (B + 16 + 4 min(B, cap - B) bytes in a
-    6 x 16 KB ring); else select_compact_kernel."""
+    4 x 16 KB ring); else select_compact_kernel."""
     B = w.budget
     bcap = -(-min(B, cap) // 32) * 32
-    total = 6 * 16384 + 96 + 1024 + 256 + 128 + -(-bcap * 4 // 128) * 128
-    hf_ok = compact != "holefill" or B + 16 + 4 * max(min(B, cap - B), 0) <= 6 * 16384
+    total = 4 * 16384 + 64 + 1024 + 256 + 128 + -(-bcap * 4 // 128) * 128
+    hf_ok = compact != "holefill" or B + 16 + 4 * max(min(B, cap - B), 0) <= 4 * 16384
     return "select2_kernel" if total <= 232448 and hf_ok else "select_compact_kernel"
 
 

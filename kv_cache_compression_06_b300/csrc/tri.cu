@@ -833,7 +833,7 @@ struct SCLayout {
 // used; every thread turns its keys into z = max_h (s_h - mean_h) / std_h and
 // writes the order-preserving keys (4 per store).  Key slots in
 // [N, round4(N)) receive don't-care values.
-template <int G>
+template <int G, bool PF = true>
 __device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *mom, uint32_t *keys) {
   constexpr int U = G >= 8 ? 1 : 8 / G;
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -846,7 +846,7 @@ __device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *
   const int n4 = (N + 3) / 4;
   const float4 *rows = reinterpret_cast<const float4 *>(raw_u);
   const int hs = capp / 4;   // float4 stride between heads
-  float4 cur[U][G], nxt[U][G];
+  float4 cur[U][G], nxt[PF ? U : 1][PF ? G : 1];
   auto load = [&](float4 (&v)[U][G], int base) {
 #pragma unroll
     for (int k = 0; k < U; ++k) {
@@ -855,9 +855,12 @@ __device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *
       for (int h = 0; h < G; ++h) v[k][h] = q < n4 ? __ldg(rows + (long long)h * hs + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
-  load(cur, tid);
+  if constexpr (PF) load(cur, tid);
   for (int base = tid; base < n4; base += nt * U) {
-    load(nxt, base + nt * U);
+    if constexpr (PF)
+      load(nxt, base + nt * U);
+    else
+      load(cur, base);
 #pragma unroll
     for (int k = 0; k < U; ++k) {
       const int q = base + k * nt;
@@ -877,10 +880,12 @@ __device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *
         reinterpret_cast<uint4 *>(keys)[q] = make_uint4(score_key(z[0]), score_key(z[1]), score_key(z[2]),
                                                         score_key(z[3]));
     }
+    if constexpr (PF) {
 #pragma unroll
-    for (int k = 0; k < U; ++k)
+      for (int k = 0; k < U; ++k)
 #pragma unroll
-      for (int h = 0; h < G; ++h) cur[k][h] = nxt[k][h];
+        for (int h = 0; h < G; ++h) cur[k][h] = nxt[k][h];
+    }
   }
 }
 
@@ -987,13 +992,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
   }
 }
 
-// ---------------------------------------------------------------- long units: select/compact, two per SM
+// ---------------------------------------------------------------- long units: select/compact, three per SM
 // The compress step's long-unit select/compact (select_compact_kernel mode 0)
-// with its keys in the workspace instead of shared memory: 256 threads, a
-// 6-stage compaction ring, ~106 KB of shared memory, so two CTAs (units) share
-// an SM and one unit's selection overlaps the other's compaction traffic.
+// with its keys in the workspace instead of shared memory: 256 threads, at
+// most 80 registers, a 4-stage compaction ring, ~70-75 KB of shared memory, so
+// three CTAs (units) share an SM and the latency-bound phases of one unit (z/max
+// loads, radix and kept-list passes over its keys in L2) overlap the others'
+// compaction traffic.  The z/max loads are single-buffered here (the extra
+// CTAs supply the memory-level parallelism).
 constexpr int kSel2Threads = 256;
-constexpr int kSel2Stages = 6;
+constexpr int kSel2Stages = 4;
 
 struct Sel2Layout {
   int bars, hist, sm, mom, idx, total;
@@ -1008,7 +1016,7 @@ struct Sel2Layout {
   }
 };
 
-__global__ void __launch_bounds__(kSel2Threads, 2) select2_kernel(const __grid_constant__ SCArgs a) {
+__global__ void __launch_bounds__(kSel2Threads, 3) select2_kernel(const __grid_constant__ SCArgs a) {
   extern __shared__ __align__(1024) char smem[];
   const Sel2Layout lay(a.bcap);
   char *ring = smem;
@@ -1053,10 +1061,10 @@ __global__ void __launch_bounds__(kSel2Threads, 2) select2_kernel(const __grid_c
   uint32_t *keys = a.keys + (long long)u * a.capp;
   const float *raw_u = a.raw + (long long)u * a.G * a.capp;
   switch (a.G) {
-    case 1: zmax_from_raw<1>(raw_u, a.capp, N, mom, keys); break;
-    case 2: zmax_from_raw<2>(raw_u, a.capp, N, mom, keys); break;
-    case 4: zmax_from_raw<4>(raw_u, a.capp, N, mom, keys); break;
-    default: zmax_from_raw<8>(raw_u, a.capp, N, mom, keys); break;
+    case 1: zmax_from_raw<1, false>(raw_u, a.capp, N, mom, keys); break;
+    case 2: zmax_from_raw<2, false>(raw_u, a.capp, N, mom, keys); break;
+    case 4: zmax_from_raw<4, false>(raw_u, a.capp, N, mom, keys); break;
+    default: zmax_from_raw<8, false>(raw_u, a.capp, N, mom, keys); break;
   }
   __syncthreads();   // the keys (global) are visible to the whole CTA
   int ntie;
@@ -1631,7 +1639,7 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   sa.idx_out = idx_out;
   sa.new_len = new_len;
   sa.keys = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + w.keys_off);
-  // two units per SM when the hole-fill bookkeeping (B bytes + 4 min(B, N - B))
+  // three units per SM when the hole-fill bookkeeping (B bytes + 4 min(B, N - B))
   // fits the smaller ring; else the one-per-SM kernel with keys in shared memory
   const Sel2Layout l2(sa.bcap);
   const int64_t movers = std::min<int64_t>(params->budget, cache->cap - params->budget);
