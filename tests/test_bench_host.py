@@ -1,0 +1,53 @@
+"""Host-side checks of bench.py that need no GPU.
+
+The bench line names the kernels a step launches; for long units that name
+follows the library's own rule for choosing select2_kernel (its shared-memory
+layout and ring size).  These tests restate that rule from the constants in the
+CUDA sources and check bench.py's copy of it, so the two cannot drift apart.
+"""
+import os
+import re
+
+import pytest
+
+import bench
+from synth import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "kv_cache_compression_06_b300", "csrc")
+
+
+def _const(name):
+    for f in ("tri.cu", "tri_device.cuh", "tri_path.cuh"):
+        with open(os.path.join(CSRC, f)) as fh:
+            m = re.search(r"constexpr int %s = (\d+);" % name, fh.read())
+        if m:
+            return int(m.group(1))
+    raise KeyError(name)
+
+
+def _rule(B, cap, compact):
+    stages, stage, sel_ints, max_smem = (_const("kSel2Stages"), _const("kStageBytes"), _const("kSelInts"),
+                                         _const("kMaxSmem"))
+    up = lambda x, a: -(-x // a) * a
+    bcap = up(min(B, cap), 32)
+    total = stages * stage + 2 * stages * 8 + 1024 + sel_ints * 4 + 128 + up(bcap * 4, 128)
+    hf_ok = compact != "holefill" or B + 16 + 4 * max(min(B, cap - B), 0) <= stages * stage
+    return "select2_kernel" if total <= max_smem and hf_ok else "select_compact_kernel"
+
+
+@pytest.mark.parametrize("B", [256, 1024, 2048, 8192, 16000, 40000])
+@pytest.mark.parametrize("cap", [2176, 32768, 65536])
+@pytest.mark.parametrize("compact", ["ordered", "holefill"])
+def test_select_kernel_name_follows_library_rule(B, cap, compact):
+    w = WORKLOADS["qwen3_8b_36l_b4_n32768"].with_(budget=B)
+    assert bench._select_kernel_name(w, cap, compact) == _rule(B, cap, compact)
+
+
+def test_moved_rows_counts_only_compressed_units():
+    import torch
+    B = 4
+    idx = torch.tensor([[[[0, 1, 2, 3]], [[0, 2, 5, 7]]]], dtype=torch.int32)   # [L=1][S=2][Hkv=1][B]
+    seq_len = torch.tensor([4, 9], dtype=torch.int32)
+    # sequence 0 has N <= B (untouched); sequence 1 keeps slot 0 in place and moves 3 rows
+    assert bench._moved_rows(idx, seq_len, B) == 3
