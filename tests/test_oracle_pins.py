@@ -191,6 +191,51 @@ def test_norm_score_special_cases_and_rotation_invariance():
         np.testing.assert_allclose(O.norm_score(R, m, rot, pairing), O.norm_score(R, m, k, pairing), rtol=1e-12)
 
 
+def test_norm_score_weight_is_linear_in_the_mean_magnitude_of_its_band():
+    """With R = 0 the norm score is sum_f m_f |k_f|: a one-hot m of value c at band
+    f gives c times the modulus of that band's (re, im) pair, and nothing from the
+    other bands.  Fails if m is dropped (the result would not scale with c), squared
+    (it would scale with c^2) or applied to the wrong band."""
+    rng = np.random.default_rng(15)
+    d, N = 16, 7
+    F = d // 2
+    k = rng.normal(size=(N, d))
+    for pairing in ["half", "interleaved"]:
+        for f in [0, 3, F - 1]:
+            for c in [0.5, 2.0, 3.0]:
+                m = np.zeros((1, F))
+                m[0, f] = c
+                got = O.norm_score(np.zeros((1, F)), m, k, pairing)[0]
+                re_i, im_i = (f, f + F) if pairing == "half" else (2 * f, 2 * f + 1)
+                want = [c * math.hypot(k[i, re_i], k[i, im_i]) for i in range(N)]
+                np.testing.assert_allclose(got, want, rtol=1e-14)
+
+
+def test_two_sample_calibration_feeds_the_norm_weight_with_R_below_one():
+    """End to end through calibrate -> compress_unit with a band that is not
+    concentrated.  One band (d = 2, omega_0 = 1 for any theta); two calibration
+    queries q_A = 2 and q_B = 4i, so center c = 1 + 2i, m = (2 + 4) / 2 = 3 and
+    R = |(1 + i) / 2| = 1/sqrt(2).  A key of modulus 1 stored post-RoPE at position
+    p = t + o with pre-RoPE phase 0 has trig score Re[c] = 1 for the single offset
+    o, so s = 1 + (1 - 1/sqrt(2)) * 3 * 1 = 1.878680...  A key of modulus 5 at the
+    same phase scores 5 + (1 - 1/sqrt(2)) * 3 * 5.  Dropping m gives 1.29 for the
+    first key; squaring it gives 3.64."""
+    q = np.zeros((2, 1, 2))
+    q[0, 0] = [2.0, 0.0]
+    q[1, 0] = [0.0, 4.0]
+    c, R, m = O.calibrate(q)
+    assert abs(c[0, 0] - (1 + 2j)) < 1e-15
+    assert abs(m[0, 0] - 3.0) < 1e-15
+    assert abs(R[0, 0] - 1 / math.sqrt(2)) < 1e-15
+    t, o, theta = 10, 3, 1e4
+    p = t + o
+    # post-RoPE keys at position p: pre-RoPE (r, 0) rotated by angle p
+    k_post = np.array([[math.cos(p), math.sin(p)], [5 * math.cos(p), 5 * math.sin(p)]])
+    res = O.compress_unit(c, R, m, k_post, np.eye(2), np.array([p, p], dtype=np.float64), t, [o], theta, 1)
+    w = (1 - 1 / math.sqrt(2)) * 3.0
+    np.testing.assert_allclose(res["s"][0], [1 + w, 5 * (1 + w)], rtol=1e-12)
+
+
 def test_norm_score_weight_falls_with_concentration():
     k = np.ones((1, 4))
     m = np.ones((1, 2))
