@@ -148,6 +148,71 @@ TRI_API tri_status tri_calibrate_stats(const void *q_pre, tri_dtype dtype, int64
                                int d, tri_pairing pairing, float *center, float *R, float *mag,
                                cudaStream_t stream);
 
+/* Streamed calibration (concentration paragraph; pipeline summary: the
+ * centers, norms and concentration are offline statistics).  The statistics
+ * of tri_calibrate_stats are means over the samples, so they are carried as
+ * sums that chunks of samples add to in any order, on any number of streams
+ * or devices, and are divided out at the end.
+ *
+ * acc: [L][H][F][TRI_CALIB_ACC_DOUBLES] fp64 (device, 8-byte aligned), per
+ * (layer, head, band): sum re q_f, sum im q_f, sum |q_f|, sum re q_f/|q_f| and
+ * sum im q_f/|q_f| over samples with |q_f| > 0, the count of those samples, the
+ * count of all samples, and one unused slot.  The caller owns it
+ * (L*H*(d/2)*TRI_CALIB_ACC_DOUBLES*8 bytes).
+ *
+ * tri_calib_reset     zeroes acc.
+ * tri_calib_accumulate adds n samples: element e of head h of sample i of layer l
+ *                     is q[l*layer_stride + i*sample_stride + h*d + e] (elements
+ *                     of dtype; sample_stride 0 means H*d, layer_stride 0 means
+ *                     n*sample_stride), e.g. the query slice of a fused QKV
+ *                     activation.  q 16-byte aligned; strides multiples of 4
+ *                     elements; sample_stride >= H*d.  n = 0 adds nothing
+ *                     (q may then be NULL).
+ *                     Accumulation is fp32 over at most 512 samples per thread
+ *                     group, then fp64 atomics: the low bits of the sums depend
+ *                     on the order in which CTAs finish.
+ * tri_calib_merge     acc += other (element-wise; e.g. partial accumulators of
+ *                     several streams or devices, copied to one device).
+ * tri_calib_finalize  writes center = sum q / count, mag = sum |q| / count,
+ *                     R = |sum q/|q|| / nonzero count (0 if none); a band with
+ *                     no samples gets 0 everywhere.  Same layouts as
+ *                     tri_calibrate_stats.
+ * All return TRI_ERR_INVALID for L < 1, H < 1, d not in {64, 128}, or bad
+ * pointers, strides or alignment. */
+#define TRI_CALIB_ACC_DOUBLES 8
+TRI_API tri_status tri_calib_reset(double *acc, int L, int H, int d, cudaStream_t stream);
+TRI_API tri_status tri_calib_accumulate(const void *q, tri_dtype dtype, int64_t n, int L, int H, int d,
+                                        tri_pairing pairing, int64_t sample_stride, int64_t layer_stride,
+                                        double *acc, cudaStream_t stream);
+TRI_API tri_status tri_calib_merge(double *acc, const double *other, int L, int H, int d,
+                                   cudaStream_t stream);
+TRI_API tri_status tri_calib_finalize(const double *acc, int L, int H, int d, float *center, float *R,
+                                      float *mag, cudaStream_t stream);
+
+/* Distance-preference curves (trig-series paragraph: with Q/K replaced by
+ * their calibrated centers the RoPE logit becomes a trigonometric series in the
+ * query-key distance, the head's distance-preference curve, reported to track
+ * the attention's distance preference with high correlation).  For query head h
+ * of layer l, KV head g = h / (Hq/Hkv), distance delta = 0..n_delta-1:
+ *   center_curve[l][h][delta] = sum_f Re[cq_{h,f} conj(ck_{g,f}) e^{i omega_f delta}]
+ *   logit_curve[l][h][delta]  = mean over i in [0, n - delta) of the RoPE logit of
+ *       query sample i + delta (position i + delta) against key sample i
+ *       (position i): sum_f Re[q_{i+delta,f} conj(k_{i,f}) e^{i omega_f delta}]
+ *   corr[l][h] = Pearson correlation of the two curves over delta (0 when
+ *       either curve is constant).
+ * q_center: [L][Hq][F][2], k_center: [L][Hkv][F][2] fp32 (e.g. tri_calibrate_stats
+ * of pre-RoPE queries and of pre-RoPE keys).  q_seq: [L][n][Hq][d], k_seq:
+ * [L][n][Hkv][d] pre-RoPE samples of one sequence (dtype, 4-byte aligned).
+ * Outputs fp32 [L][Hq][n_delta] and [L][Hq].  logit_curve and corr may be NULL
+ * (then q_seq, k_seq are not read; corr needs logit_curve).  The phase
+ * omega_f*delta is reduced modulo 2*pi in fp64.  Requires n_delta >= 1, and
+ * n_delta <= n when the logit curve is asked for. */
+TRI_API tri_status tri_distance_curves(const float *q_center, const float *k_center, const void *q_seq,
+                                       const void *k_seq, tri_dtype dtype, int64_t n, int L, int Hq, int Hkv,
+                                       int d, double theta, tri_pairing pairing, int n_delta,
+                                       float *center_curve, float *logit_curve, float *corr,
+                                       cudaStream_t stream);
+
 /* Workspace bytes that tri_score / tri_compress_step need for these arguments
  * (0 when every unit fits one CTA's shared memory).  `bytes` is a host pointer. */
 TRI_API tri_status tri_workspace_bytes(const tri_cache *cache, const tri_stats *stats,
@@ -169,7 +234,9 @@ TRI_API tri_status tri_score(const tri_cache *cache, const tri_stats *stats, con
 TRI_API tri_status tri_select_topb(const tri_cache *cache, const float *agg, int budget, int32_t *idx,
                            void *ws, size_t ws_bytes, cudaStream_t stream);
 
-/* In-place compaction of every unit with N > budget to its kept slots
+/* In-place compaction (pruning paragraph: the top B keys are kept, the rest
+ * of the unit's keys are dropped from the cache) of every unit with N > budget
+ * to its kept slots
  * idx[u][0..budget) (as tri_select_topb writes them: strictly increasing in
  * [0, N), checked on the device: a bad row skips its unit and records
  * TRI_ERR_INVALID).  ORDERED: row j of K and V becomes row idx[u][j];
@@ -179,8 +246,11 @@ TRI_API tri_status tri_select_topb(const tri_cache *cache, const float *agg, int
 TRI_API tri_status tri_compact_kv(const tri_cache *cache, const int32_t *idx, int budget,
                           tri_compact_mode mode, int32_t *new_len, cudaStream_t stream);
 
-/* The fused step: score -> GQA z/max -> top-B -> in-place compaction for every
- * unit with N > budget (units with N <= budget untouched).
+/* The fused step (pruning paragraph: every 128 generated tokens, when the
+ * cache exceeds the budget, score every key, z-score per query head and take
+ * the max per KV head, keep the top B): score -> GQA z/max -> top-B -> in-place
+ * compaction for every unit with N > budget (units with N <= budget untouched).
+ * The caller makes the call at its 128-token boundaries.
  * idx_out: NULL or [L][S][Hkv][budget] int32: the original slot of the row now
  * at each slot j < budget (ORDERED: the kept slots ascending, as
  * tri_select_topb writes them; HOLEFILL: j for kept slots below B, the mover
@@ -211,7 +281,11 @@ TRI_API tri_status tri_compress_step(const tri_cache *cache, const tri_stats *st
  *
  * Set-up: the first call on each device looks up that device's address of the
  * array (with that device current), so make that first call before any stream
- * capture begins.  A failed lookup returns TRI_ERR_CUDA.
+ * capture begins.  A failed lookup returns TRI_ERR_CUDA.  The address is kept
+ * per device together with the CUDA context that was current at the lookup; a
+ * call under another context (after cudaDeviceReset, or with a context the
+ * caller made current) looks the address up again, so again make such a call
+ * outside any stream capture.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents; the step writes each scratch entry before reading it, so
@@ -222,6 +296,53 @@ TRI_API tri_status tri_compress_step_static_scratch(const tri_cache *cache, cons
                                             const tri_params *params, tri_compact_mode mode,
                                             int32_t *idx_out, int32_t *new_len,
                                             cudaStream_t stream);
+
+/* Decode loop around the compression step (pruning paragraph: during online
+ * decoding the step runs once every 128 generated tokens when the cache exceeds
+ * the budget).  These calls are the decode side of that loop: they are not part
+ * of the compression method, they let it run inside a decode loop on the same
+ * cache.  A loop appends a token to every unit, attends, and every 128 tokens
+ * calls tri_compress_step with t = the next query position.
+ *
+ * tri_append_kv: k_new, v_new [L][S][Hkv][d] (cache dtype, 16-byte aligned):
+ *   the new token's pre-RoPE key and its value for every unit.  The key is
+ *   rotated to position pos[s] (band f times e^{i omega_f pos[s]}, the phase
+ *   reduced modulo 2 pi in fp64, rounded to the cache dtype) and written with
+ *   the value into slot N = seq_len[s] of unit (l, s, g) (paged: block
+ *   block_table[s][N / block], row N % block).  seq_len_out[s] receives N + 1 and
+ *   pos_out[s] (NULL: not written) pos[s] + 1.  Neither may alias seq_len or
+ *   pos.  A sequence whose slot N is not available (N >= cap, or its block id
+ *   out of range) is skipped with TRI_ERR_BOUNDS in the device status and
+ *   seq_len_out[s] = N, pos_out[s] = pos[s].
+ * tri_decode_workspace_bytes: scratch that tri_decode_attention needs (0 when
+ *   one CTA per unit suffices; otherwise per-slice partial results).
+ * tri_decode_attention: q [L][S][Hq][d] bf16 pre-RoPE queries (one per
+ *   sequence and query head), rotated to pos[s] inside; for query head h of
+ *   unit (l, s, g = h / (Hq/Hkv)):
+ *     out[l][s][h] = sum_{i < N} w_i v_i,  w = softmax_i(scale * q~_h . k~_i)
+ *   over the unit's N = seq_len[s] slots, out fp32 [L][S][Hq][d].  The slot
+ *   order does not matter (ordered or hole-fill compaction give the same
+ *   output).  bf16 caches only (TRI_ERR_UNSUPPORTED otherwise), G in {1, 2, 4,
+ *   8}.  Both products run on the tensor cores with the query and the
+ *   probabilities split into bf16 hi + lo parts and fp32 accumulation.  A unit
+ *   with N = 0 gets out = 0. */
+TRI_API tri_status tri_append_kv(const tri_cache *cache, const void *k_new, const void *v_new,
+                                 const int32_t *pos, double theta, tri_pairing pairing,
+                                 int32_t *seq_len_out, int32_t *pos_out, cudaStream_t stream);
+TRI_API tri_status tri_decode_workspace_bytes(const tri_cache *cache, int Hq, size_t *bytes);
+TRI_API tri_status tri_decode_attention(const tri_cache *cache, const void *q, int Hq, const int32_t *pos,
+                                        double theta, tri_pairing pairing, float scale, float *out,
+                                        void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Health check of the bounded-wait path: launches one warp whose thread 0
+ * waits on a shared-memory barrier that nothing arrives at, with a limit of
+ * limit_us microseconds (1..1000000); nothing else is in flight.  The wait
+ * gives up, records TRI_ERR_TIMEOUT in the device status word and the kernel
+ * returns, after which the kernels of later calls return without work until
+ * tri_clear_device_status() (exactly as after a wait that gave up inside a
+ * step).  Lets a caller confirm that a stuck wait ends with a status, not a
+ * hang.  Not part of the method. */
+TRI_API tri_status tri_check_bounded_wait(uint32_t limit_us, cudaStream_t stream);
 
 /* Reads (and synchronises `stream` for) the device status word; *out (host)
  * receives TRI_OK or the first device-side error recorded since the last clear. */

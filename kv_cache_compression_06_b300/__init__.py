@@ -19,4 +19,8 @@ from .tri import (  # noqa: F401
     tri_version,
     tri_workspace_bytes,
     workspace,
+    tri_append_kv,
+    tri_decode_attention,
+    tri_decode_workspace_bytes,
 )
+from .decode import DecodeLoop  # noqa: F401

@@ -8,7 +8,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SRC = os.path.join(PKG, "csrc", "tri.cu")
 OUT = os.path.join(PKG, "libtri.so")
-DEPS = [os.path.join(PKG, "csrc", f) for f in ("tri.cu", "tri_device.cuh", "tri_path.cuh", "tri_mma.cuh")] + [
+CSRC = ("tri.cu", "tri_device.cuh", "tri_path.cuh", "tri_mma.cuh", "tri_calib.cuh", "tri_curve.cuh", "tri_decode.cuh")
+DEPS = [os.path.join(PKG, "csrc", f) for f in CSRC] + [
     os.path.join(ROOT, "include", "tri.h")]
 
 

@@ -16,6 +16,15 @@
 //   zmax_kernel          a3 for long units (tri_score): Chan-merged moments -> agg.
 //   select_compact_kernel a3..a5 for long units (from raw scores), tri_select_topb
 //                        (from agg) and tri_compact_kv (from idx).
+//   calib_*_kernel       streamed calibration: sums per (layer, head, band) that
+//                        chunks of samples add to, merged, then finalised.
+//   *_curve_kernel       distance-preference curves (centers vs exact logits).
+//   wait_check_kernel    a bounded wait that gives up (health check of the
+//                        timeout path).
+//   append_kv_kernel     decode loop: one token's K (rotated to its position)
+//                        and V into slot N of every unit.
+//   decode_attn_kernel   decode loop: single-query attention over the cache
+//                        (split-K, tensor cores), decode_merge_kernel merges splits.
 #include <cmath>
 #include <cstdio>
 #include <algorithm>
@@ -23,6 +32,9 @@
 #include <mutex>
 
 #include "tri_mma.cuh"
+#include "tri_calib.cuh"
+#include "tri_curve.cuh"
+#include "tri_decode.cuh"
 
 namespace tri {
 
@@ -351,37 +363,6 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
 #pragma unroll
     for (int h = 0; h < G; ++h)
       a.part[((long long)u * a.ntiles + tile) * G + h] = make_float2(mu[h], m2[h]);
-  }
-}
-
-// Loads rows [row0, row0 + nrows) of unit (l, s, g)'s K into a swizzled stage
-// of kStageBytes (two boxes of 64 elements per row for d = 128, one for d = 64).
-// Dense: the unit's slot 0 is row urow0 of the 2-D view; rows past the unit are
-// loaded too and never scored, rows past the tensor read as zero.  Paged: one
-// copy per block and half.  Called by all lanes of the producer warp.
-template <int D>
-__device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUtensorMap *map, int l, int s,
-                                                 int g, long long urow0, int row0, int nrows, char *dst,
-                                                 uint64_t *full, int lane) {
-  constexpr int TR = kStageBytes / (2 * D), NH = D / 64;   // rows per stage, halves per row
-  if (!c.paged()) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(full, (uint32_t)kStageBytes);
-#pragma unroll
-      for (int hh = 0; hh < NH; ++hh) tma_load_2d(dst + hh * TR * 128, map, 64 * hh, (int)(urow0 + row0), full);
-    }
-    return;
-  }
-  const int blk = c.block, nblk = (nrows + blk - 1) / blk;
-  if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nblk * blk * 128 * NH));
-  __syncwarp();
-  if (lane < nblk) {
-    const int b = c.bt[(long long)s * c.max_blocks + row0 / blk + lane];
-    const int z = (int)((long long)l * c.nblocks + b);
-    if constexpr (NH == 2)
-      tma_load_5d(dst + lane * blk * 256, map, 0, 0, 0, g, z, full);   // [half][blk rows] of one block
-    else
-      tma_load_4d(dst + lane * blk * 128, map, 0, g, 0, z, full);
   }
 }
 
@@ -1205,15 +1186,15 @@ static bool make_row_map(const tri_cache *c, void *base, CUtensorMap *map) {
   return r == CUDA_SUCCESS;
 }
 
-// 128B-swizzled K map for the tensor-core score kernel (bf16, rotate-half, d in
+// 128B-swizzled map of K or V (`base`) for the tensor-core kernels (bf16, d in
 // {64, 128}): dense, a 2-D view [rows][d] with boxes of 64 elements x one
 // stage of rows; paged, the 4-D pool view with boxes of 64 elements x one block
 // of one head (a stage must hold a whole number of blocks, at most 32).
-static bool make_swizzled_map(const tri_cache *c, const tri_params *p, CUtensorMap *map) {
-  if (c->dtype != TRI_BF16 || p->pairing != TRI_PAIR_HALF || (c->d != 64 && c->d != 128)) return false;
+static bool make_sw_map(const tri_cache *c, void *base, CUtensorMap *map) {
+  if (c->dtype != TRI_BF16 || (c->d != 64 && c->d != 128)) return false;
   const int rb = c->d * 2, tr = kStageBytes / rb;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (enc == nullptr || c->k == nullptr) return false;
+  if (enc == nullptr || base == nullptr) return false;
   CUresult r;
   if (c->block_table == nullptr) {
     const int64_t rows = (int64_t)c->L * c->S * c->Hkv * c->cap;
@@ -1222,7 +1203,7 @@ static bool make_swizzled_map(const tri_cache *c, const tri_params *p, CUtensorM
     const cuuint64_t strides[1] = {(cuuint64_t)rb};
     const cuuint32_t box[2] = {64u, (cuuint32_t)tr};
     const cuuint32_t estr[2] = {1u, 1u};
-    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->k, dims, strides, box, estr,
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else if (c->d == 128) {
@@ -1236,7 +1217,7 @@ static bool make_swizzled_map(const tri_cache *c, const tri_params *p, CUtensorM
                                    (cuuint64_t)c->block * c->Hkv * rb};
     const cuuint32_t box[5] = {64u, (cuuint32_t)c->block, 2u, 1u, 1u};
     const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
-    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, c->k, dims, strides, box, estr,
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
@@ -1247,11 +1228,16 @@ static bool make_swizzled_map(const tri_cache *c, const tri_params *p, CUtensorM
     const cuuint64_t strides[3] = {(cuuint64_t)rb, (cuuint64_t)c->Hkv * rb, (cuuint64_t)c->block * c->Hkv * rb};
     const cuuint32_t box[4] = {64u, 1u, (cuuint32_t)c->block, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, c->k, dims, strides, box, estr,
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
   return r == CUDA_SUCCESS;
+}
+
+// The score kernels' K map: bf16 caches with rotate-half bands only.
+static bool make_swizzled_map(const tri_cache *c, const tri_params *p, CUtensorMap *map) {
+  return p->pairing == TRI_PAIR_HALF && make_sw_map(c, c->k, map);
 }
 
 // Builds the tensor maps of a call and sets the view's flags.  K and V maps
@@ -1436,6 +1422,74 @@ static int bcap_of(const tri_cache *c, int budget) {
   return round32(budget < c->cap ? budget : c->cap);
 }
 
+// ---------------------------------------------------------------- calibration streaming, curves
+template <int D, bool BF16, bool INTER>
+static tri_status run_calib_acc(const char *q, long long n, long long ss, long long ls, int L, int H,
+                                double *acc, cudaStream_t st) {
+  constexpr long long kMaxZ = 65535;
+  const int es = BF16 ? 2 : 4;
+  for (long long i0 = 0; i0 < n; i0 += kMaxZ * kCalibChunk) {
+    const long long m = std::min(n - i0, kMaxZ * kCalibChunk);
+    const unsigned z = (unsigned)((m + kCalibChunk - 1) / kCalibChunk);
+    calib_accumulate_kernel<D, BF16, INTER><<<dim3((unsigned)H, (unsigned)L, z), kCalibThreads, 0, st>>>(
+        q + i0 * ss * es, m, ss, ls, H, acc);
+    if (cudaGetLastError() != cudaSuccess) return TRI_ERR_CUDA;
+  }
+  return TRI_OK;
+}
+
+template <int D, bool BF16, bool INTER>
+static tri_status run_logit_curve(const void *q, const void *k, long long n, int L, int Hq, int Hkv, int n_delta,
+                                  const StepConst &sc, float *curve, cudaStream_t st) {
+  const unsigned gx = (unsigned)((n_delta + kCurveDeltas - 1) / kCurveDeltas);
+  logit_curve_kernel<D, BF16, INTER><<<dim3(gx, (unsigned)Hq, (unsigned)L), kCurveThreads, 0, st>>>(
+      q, k, n, Hq, Hkv, n_delta, sc, curve);
+  return launch_result();
+}
+
+// Phase-only constants (omega_f; Phi unused) for the curve kernels.
+static StepConst omega_const(double theta, int d) {
+  StepConst sc;
+  std::memset(&sc, 0, sizeof(sc));
+  for (int f = 0; f < d / 2; ++f) sc.omega[f] = std::pow(theta, -2.0 * f / (double)d);
+  return sc;
+}
+
+__global__ void __launch_bounds__(32) wait_check_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // nothing arrives on the barrier: its phase 0 never completes and the wait
+  // gives up after limit_ns (nothing is in flight)
+  if (threadIdx.x == 0) mbar_wait_for(&bar, 0, limit_ns);
+}
+
+// ---------------------------------------------------------------- decode loop
+// Slices per unit for the decode attention: enough CTAs for two waves of two
+// per SM, slices of at most 8192 keys, at least one stage of rows each.
+static int decode_splits(const tri_cache *c) {
+  const int tr = kStageBytes / (2 * c->d);
+  const int64_t units = units_of(c);
+  int64_t n = std::max<int64_t>((2 * 148 * 2 + units - 1) / units, (c->cap + 8191) / 8192);
+  n = std::min<int64_t>(n, (c->cap + tr - 1) / tr);
+  return (int)std::max<int64_t>(1, std::min<int64_t>(n, 65535));
+}
+
+template <int D, int G>
+static tri_status run_decode(const DecodeArgs &a, int64_t units, cudaStream_t st) {
+  const DecLayout lay(G, D);
+  auto k = decode_attn_kernel<D, G>;
+  if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
+  k<<<dim3((unsigned)a.nsplit, (unsigned)units), kDecThreads, lay.total, st>>>(a);
+  tri_status e = launch_result();
+  if (e != TRI_OK || a.nsplit == 1) return e;
+  decode_merge_kernel<<<(unsigned)units, 256, 0, st>>>(a.part, a.nsplit, G, D, a.c.S, a.c.Hkv, a.Hq, a.out);
+  return launch_result();
+}
+
 // ---------------------------------------------------------------- built-in scratch
 // Scratch of tri_compress_step_static_scratch, for callers that cannot
 // allocate.  In host code `g_static_scratch` names a host-side stand-in, not
@@ -1445,19 +1499,44 @@ static __device__ __align__(256) unsigned char g_static_scratch[TRI_STATIC_SCRAT
 constexpr int kMaxDevices = 64;
 static std::mutex g_static_mu;
 static void *g_static_addr[kMaxDevices];
+static CUcontext g_static_ctx[kMaxDevices];
 
-// Device address of g_static_scratch on the current device, looked up once per
-// device (with that device current) and cached.
+// cuCtxGetCurrent from the driver, looked up once (no link against libcuda).
+static PFN_cuCtxGetCurrent_v4000 ctx_getter() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  return fn;
+}
+
+// Device address of g_static_scratch on the current device, looked up with
+// that device current and cached together with the context that was current
+// then.  A call under another context (after a device reset, or a context the
+// caller made current) looks the address up again: a cached address belongs to
+// the context it was taken in.
 static tri_status static_scratch_addr(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return TRI_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return TRI_ERR_UNSUPPORTED;
+  PFN_cuCtxGetCurrent_v4000 get = ctx_getter();
+  if (get == nullptr) return TRI_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return TRI_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (g_static_addr[dev] == nullptr) {
+  if (ctx == nullptr || g_static_addr[dev] == nullptr || g_static_ctx[dev] != ctx) {
+    // the lookup also binds the runtime's context for this device when none
+    // is current yet; the context is read again after it
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
-      return TRI_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return TRI_ERR_CUDA;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return TRI_ERR_CUDA;
     g_static_addr[dev] = p;
+    g_static_ctx[dev] = ctx;
   }
   *out = g_static_addr[dev];
   return TRI_OK;
@@ -1667,6 +1746,198 @@ tri_status tri_compress_step_static_scratch(const tri_cache *cache, const tri_st
   if ((e = static_scratch_addr(&ws)) != TRI_OK) return e;
   return tri_compress_step(cache, stats, params, mode, idx_out, new_len, ws,
                            (size_t)TRI_STATIC_SCRATCH_BYTES, stream);
+}
+
+static tri_status check_calib_shape(int L, int H, int d) {
+  if (L < 1 || H < 1) return TRI_ERR_INVALID;
+  if (d != 64 && d != 128) return TRI_ERR_INVALID;
+  return TRI_OK;
+}
+static long long calib_doubles(int L, int H, int d) { return (long long)L * H * (d / 2) * kCalibAcc; }
+static unsigned grid_for(long long count) {
+  return (unsigned)std::max<long long>(1, std::min<long long>((count + 255) / 256, 148 * 8));
+}
+
+tri_status tri_calib_reset(double *acc, int L, int H, int d, cudaStream_t stream) {
+  tri_status e;
+  if ((e = check_calib_shape(L, H, d)) != TRI_OK) return e;
+  if (acc == nullptr || (reinterpret_cast<uintptr_t>(acc) & 7u)) return TRI_ERR_INVALID;
+  const long long cnt = calib_doubles(L, H, d);
+  calib_zero_kernel<<<grid_for(cnt), 256, 0, stream>>>(acc, cnt);
+  return launch_result();
+}
+
+tri_status tri_calib_accumulate(const void *q, tri_dtype dtype, int64_t n, int L, int H, int d,
+                                tri_pairing pairing, int64_t sample_stride, int64_t layer_stride, double *acc,
+                                cudaStream_t stream) {
+  tri_status e;
+  if ((e = check_calib_shape(L, H, d)) != TRI_OK) return e;
+  if (acc == nullptr || (reinterpret_cast<uintptr_t>(acc) & 7u)) return TRI_ERR_INVALID;
+  if (n < 0 || sample_stride < 0 || layer_stride < 0) return TRI_ERR_INVALID;
+  if (dtype != TRI_F32 && dtype != TRI_BF16) return TRI_ERR_INVALID;
+  if (pairing != TRI_PAIR_HALF && pairing != TRI_PAIR_INTERLEAVED) return TRI_ERR_INVALID;
+  const long long ss = sample_stride ? sample_stride : (long long)H * d;
+  const long long ls = layer_stride ? layer_stride : n * ss;
+  if (ss < (long long)H * d || (ss & 3) || (ls & 3)) return TRI_ERR_INVALID;
+  if (H > 65535 || L > 65535) return TRI_ERR_UNSUPPORTED;
+  if (n == 0) return TRI_OK;   // nothing is read (q may be NULL)
+  if (q == nullptr || !aligned16(q)) return TRI_ERR_INVALID;
+  const char *qc = static_cast<const char *>(q);
+  const bool bf = dtype == TRI_BF16, in = pairing == TRI_PAIR_INTERLEAVED;
+  switch ((d == 128 ? 4 : 0) + (bf ? 2 : 0) + (in ? 1 : 0)) {
+    case 0: return run_calib_acc<64, false, false>(qc, n, ss, ls, L, H, acc, stream);
+    case 1: return run_calib_acc<64, false, true>(qc, n, ss, ls, L, H, acc, stream);
+    case 2: return run_calib_acc<64, true, false>(qc, n, ss, ls, L, H, acc, stream);
+    case 3: return run_calib_acc<64, true, true>(qc, n, ss, ls, L, H, acc, stream);
+    case 4: return run_calib_acc<128, false, false>(qc, n, ss, ls, L, H, acc, stream);
+    case 5: return run_calib_acc<128, false, true>(qc, n, ss, ls, L, H, acc, stream);
+    case 6: return run_calib_acc<128, true, false>(qc, n, ss, ls, L, H, acc, stream);
+    default: return run_calib_acc<128, true, true>(qc, n, ss, ls, L, H, acc, stream);
+  }
+}
+
+tri_status tri_calib_merge(double *acc, const double *other, int L, int H, int d, cudaStream_t stream) {
+  tri_status e;
+  if ((e = check_calib_shape(L, H, d)) != TRI_OK) return e;
+  if (acc == nullptr || other == nullptr || acc == other) return TRI_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(acc) & 7u) || (reinterpret_cast<uintptr_t>(other) & 7u)) return TRI_ERR_INVALID;
+  const long long cnt = calib_doubles(L, H, d);
+  calib_add_kernel<<<grid_for(cnt), 256, 0, stream>>>(acc, other, cnt);
+  return launch_result();
+}
+
+tri_status tri_calib_finalize(const double *acc, int L, int H, int d, float *center, float *R, float *mag,
+                              cudaStream_t stream) {
+  tri_status e;
+  if ((e = check_calib_shape(L, H, d)) != TRI_OK) return e;
+  if (acc == nullptr || center == nullptr || R == nullptr || mag == nullptr) return TRI_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(acc) & 7u) return TRI_ERR_INVALID;
+  const long long bands = (long long)L * H * (d / 2);
+  calib_finalize_kernel<<<grid_for(bands), 256, 0, stream>>>(acc, bands, center, R, mag);
+  return launch_result();
+}
+
+tri_status tri_distance_curves(const float *q_center, const float *k_center, const void *q_seq, const void *k_seq,
+                               tri_dtype dtype, int64_t n, int L, int Hq, int Hkv, int d, double theta,
+                               tri_pairing pairing, int n_delta, float *center_curve, float *logit_curve,
+                               float *corr, cudaStream_t stream) {
+  if (L < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return TRI_ERR_INVALID;
+  if (d != 64 && d != 128) return TRI_ERR_INVALID;
+  if (!(theta > 0.0) || !std::isfinite(theta)) return TRI_ERR_INVALID;
+  if (dtype != TRI_F32 && dtype != TRI_BF16) return TRI_ERR_INVALID;
+  if (pairing != TRI_PAIR_HALF && pairing != TRI_PAIR_INTERLEAVED) return TRI_ERR_INVALID;
+  if (n_delta < 1 || q_center == nullptr || k_center == nullptr || center_curve == nullptr) return TRI_ERR_INVALID;
+  const bool want_logit = logit_curve != nullptr || corr != nullptr;
+  if (want_logit && (q_seq == nullptr || k_seq == nullptr || logit_curve == nullptr)) return TRI_ERR_INVALID;
+  if (want_logit && (n < 1 || n_delta > n)) return TRI_ERR_INVALID;
+  if (Hq > 65535 || L > 65535) return TRI_ERR_UNSUPPORTED;
+  const StepConst sc = omega_const(theta, d);
+  center_curve_kernel<<<dim3((unsigned)Hq, (unsigned)L), 256, 0, stream>>>(q_center, k_center, Hq, Hkv, d / 2,
+                                                                            n_delta, sc, center_curve);
+  tri_status e;
+  if ((e = launch_result()) != TRI_OK) return e;
+  if (!want_logit) return TRI_OK;
+  const bool bf = dtype == TRI_BF16, in = pairing == TRI_PAIR_INTERLEAVED;
+  switch ((d == 128 ? 4 : 0) + (bf ? 2 : 0) + (in ? 1 : 0)) {
+    case 0: e = run_logit_curve<64, false, false>(q_seq, k_seq, n, L, Hq, Hkv, n_delta, sc, logit_curve, stream); break;
+    case 1: e = run_logit_curve<64, false, true>(q_seq, k_seq, n, L, Hq, Hkv, n_delta, sc, logit_curve, stream); break;
+    case 2: e = run_logit_curve<64, true, false>(q_seq, k_seq, n, L, Hq, Hkv, n_delta, sc, logit_curve, stream); break;
+    case 3: e = run_logit_curve<64, true, true>(q_seq, k_seq, n, L, Hq, Hkv, n_delta, sc, logit_curve, stream); break;
+    case 4: e = run_logit_curve<128, false, false>(q_seq, k_seq, n, L, Hq, Hkv, n_delta, sc, logit_curve, stream); break;
+    case 5: e = run_logit_curve<128, false, true>(q_seq, k_seq, n, L, Hq, Hkv, n_delta, sc, logit_curve, stream); break;
+    case 6: e = run_logit_curve<128, true, false>(q_seq, k_seq, n, L, Hq, Hkv, n_delta, sc, logit_curve, stream); break;
+    default: e = run_logit_curve<128, true, true>(q_seq, k_seq, n, L, Hq, Hkv, n_delta, sc, logit_curve, stream); break;
+  }
+  if (e != TRI_OK || corr == nullptr) return e;
+  curve_corr_kernel<<<(unsigned)((long long)L * Hq), 256, 0, stream>>>(center_curve, logit_curve, n_delta, corr);
+  return launch_result();
+}
+
+tri_status tri_append_kv(const tri_cache *cache, const void *k_new, const void *v_new, const int32_t *pos,
+                         double theta, tri_pairing pairing, int32_t *seq_len_out, int32_t *pos_out,
+                         cudaStream_t stream) {
+  tri_status e;
+  if ((e = check_cache(cache, true, true)) != TRI_OK) return e;
+  if (k_new == nullptr || v_new == nullptr || pos == nullptr || seq_len_out == nullptr) return TRI_ERR_INVALID;
+  if (!aligned16(k_new) || !aligned16(v_new)) return TRI_ERR_INVALID;
+  if (seq_len_out == cache->seq_len || pos_out == pos || (pos_out != nullptr && pos_out == cache->seq_len) ||
+      reinterpret_cast<const void *>(seq_len_out) == reinterpret_cast<const void *>(pos))
+    return TRI_ERR_INVALID;
+  if (!(theta > 0.0) || !std::isfinite(theta)) return TRI_ERR_INVALID;
+  if (pairing != TRI_PAIR_HALF && pairing != TRI_PAIR_INTERLEAVED) return TRI_ERR_INVALID;
+  AppendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.c = make_view(cache);
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.pos = pos;
+  a.seq_len_out = seq_len_out;
+  a.pos_out = pos_out;
+  a.inter = pairing == TRI_PAIR_INTERLEAVED;
+  a.sc = omega_const(theta, cache->d);
+  const unsigned units = (unsigned)units_of(cache);
+  if (cache->dtype == TRI_BF16)
+    append_kv_kernel<true><<<units, 32, 0, stream>>>(a);
+  else
+    append_kv_kernel<false><<<units, 32, 0, stream>>>(a);
+  return launch_result();
+}
+
+tri_status tri_decode_workspace_bytes(const tri_cache *cache, int Hq, size_t *bytes) {
+  if (bytes == nullptr) return TRI_ERR_INVALID;
+  tri_status e;
+  if ((e = check_cache(cache, false, false)) != TRI_OK) return e;
+  if (Hq < 1 || Hq % cache->Hkv != 0) return TRI_ERR_INVALID;
+  const int G = Hq / cache->Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return TRI_ERR_UNSUPPORTED;
+  const int ns = decode_splits(cache);
+  *bytes = ns == 1 ? 0 : (size_t)units_of(cache) * ns * G * (cache->d + 2) * sizeof(float);
+  return TRI_OK;
+}
+
+tri_status tri_decode_attention(const tri_cache *cache, const void *q, int Hq, const int32_t *pos, double theta,
+                                tri_pairing pairing, float scale, float *out, void *ws, size_t ws_bytes,
+                                cudaStream_t stream) {
+  tri_status e;
+  if ((e = check_cache(cache, true, true)) != TRI_OK) return e;
+  if (q == nullptr || pos == nullptr || out == nullptr) return TRI_ERR_INVALID;
+  if (!(theta > 0.0) || !std::isfinite(theta) || !(scale > 0.f) || !std::isfinite(scale)) return TRI_ERR_INVALID;
+  if (pairing != TRI_PAIR_HALF && pairing != TRI_PAIR_INTERLEAVED) return TRI_ERR_INVALID;
+  size_t need = 0;
+  if ((e = tri_decode_workspace_bytes(cache, Hq, &need)) != TRI_OK) return e;
+  if (cache->dtype != TRI_BF16) return TRI_ERR_UNSUPPORTED;
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned16(ws))) return TRI_ERR_WORKSPACE;
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.c = make_view(cache);
+  if (!make_sw_map(cache, cache->k, &a.kmap) || !make_sw_map(cache, cache->v, &a.vmap)) return TRI_ERR_UNSUPPORTED;
+  a.q = q;
+  a.pos = pos;
+  a.Hq = Hq;
+  a.nsplit = decode_splits(cache);
+  a.inter = pairing == TRI_PAIR_INTERLEAVED;
+  a.qscale = scale * 1.4426950408889634f;
+  a.out = out;
+  a.part = static_cast<float *>(ws);
+  a.sc = omega_const(theta, cache->d);
+  const int G = Hq / cache->Hkv;
+  const int64_t units = units_of(cache);
+  switch (cache->d * 10 + G) {
+    case 641: return run_decode<64, 1>(a, units, stream);
+    case 642: return run_decode<64, 2>(a, units, stream);
+    case 644: return run_decode<64, 4>(a, units, stream);
+    case 648: return run_decode<64, 8>(a, units, stream);
+    case 1281: return run_decode<128, 1>(a, units, stream);
+    case 1282: return run_decode<128, 2>(a, units, stream);
+    case 1284: return run_decode<128, 4>(a, units, stream);
+    default: return run_decode<128, 8>(a, units, stream);
+  }
+}
+
+tri_status tri_check_bounded_wait(uint32_t limit_us, cudaStream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000u) return TRI_ERR_INVALID;
+  wait_check_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_us * 1000ull);
+  return launch_result();
 }
 
 tri_status tri_get_device_status(cudaStream_t stream, int32_t *out) {

@@ -80,20 +80,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with `parity` to complete.  Gives up after kWaitLimitNs,
+// Waits for the phase with `parity` to complete.  Gives up after limit_ns,
 // records TRI_ERR_TIMEOUT and returns false (the caller then leaves the CTA).
-__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __noinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
 #pragma unroll 1
     for (int k = 0; k < 64; ++k)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       set_status(TRI_ERR_TIMEOUT);
       return false;
     }
   }
+}
+// The kernels' wait: mbar_wait_for with the library's limit (kWaitLimitNs).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- bulk copy (TMA, untiled)

@@ -34,6 +34,13 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t &r0, uint32_t &r1, uint32_t
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
+// ldmatrix_x4 with each 8x8 matrix transposed on the way to the registers.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                                  uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
 
 // D += A * B for one m16n8k16 tile (A 16x16 row-major bf16, B 16x8 bf16, fp32 D).
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -167,6 +174,57 @@ __device__ __forceinline__ SwRow sw_row(int row, int blk) {
 // Byte address of element column `col` (a multiple of 8) of that row.
 __device__ __forceinline__ uint32_t sw_addr(uint32_t stage, const SwRow &r, int col) {
   return stage + (uint32_t)(r.off + (col >> 6) * r.hstride + ((((col & 63) >> 3) ^ r.key) << 4));
+}
+
+// Bytes that issue_stage_sw's copies of rows [row0, row0 + nrows) deliver (a
+// dense stage always carries its whole box; rows past the tensor read as zero).
+template <int D>
+__device__ __forceinline__ uint32_t stage_sw_bytes(const CacheView &c, int nrows) {
+  constexpr int NH = D / 64;
+  if (!c.paged()) return (uint32_t)kStageBytes;
+  const int blk = c.block, nblk = (nrows + blk - 1) / blk;
+  return (uint32_t)(nblk * blk * 128 * NH);
+}
+
+// Issues the tensor copies of rows [row0, row0 + nrows) of unit (l, s, g) of
+// the tensor behind `map` into a swizzled stage of kStageBytes (two boxes of
+// 64 elements per row for d = 128, one for d = 64), completing on `full`; the
+// caller has announced the bytes.  Dense: the unit's slot 0 is row urow0 of the
+// 2-D view; rows past the unit are loaded too, rows past the tensor read as
+// zero.  Paged: one copy per block carrying both halves.  All lanes of the
+// calling warp take part.
+template <int D>
+__device__ __forceinline__ void issue_stage_sw(const CacheView &c, const CUtensorMap *map, int l, int s, int g,
+                                               long long urow0, int row0, int nrows, char *dst, uint64_t *full,
+                                               int lane) {
+  constexpr int TR = kStageBytes / (2 * D), NH = D / 64;   // rows per stage, halves per row
+  if (!c.paged()) {
+    if (lane == 0) {
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) tma_load_2d(dst + hh * TR * 128, map, 64 * hh, (int)(urow0 + row0), full);
+    }
+    return;
+  }
+  const int blk = c.block, nblk = (nrows + blk - 1) / blk;
+  if (lane < nblk) {
+    const int b = c.bt[(long long)s * c.max_blocks + row0 / blk + lane];
+    const int z = (int)((long long)l * c.nblocks + b);
+    if constexpr (NH == 2)
+      tma_load_5d(dst + lane * blk * 256, map, 0, 0, 0, g, z, full);   // [half][blk rows] of one block
+    else
+      tma_load_4d(dst + lane * blk * 128, map, 0, g, 0, z, full);
+  }
+}
+
+// One stage of K for the score kernels: the arrival with its byte count, then
+// the copies.  Called by all lanes of the producer warp.
+template <int D>
+__device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUtensorMap *map, int l, int s,
+                                                 int g, long long urow0, int row0, int nrows, char *dst,
+                                                 uint64_t *full, int lane) {
+  if (lane == 0) mbar_arrive_expect_tx(full, stage_sw_bytes<D>(c, nrows));
+  __syncwarp();
+  issue_stage_sw<D>(c, map, l, s, g, urow0, row0, nrows, dst, full, lane);
 }
 
 // Scores the 16 keys at stage rows [r0, r0 + 16) (row0 + r0 + i is the key's

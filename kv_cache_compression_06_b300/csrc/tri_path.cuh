@@ -76,18 +76,24 @@ struct CacheView {
 // The phase omega_f*t is reduced modulo 2*pi in fp64 (two-term 2*pi split)
 // before an fp32 sincos: omega_0*t reaches ~3e4 rad, far beyond fp32 phase
 // accuracy.
-__device__ __forceinline__ float2 step_phase(const StepConst &sc, int f, int t) {
+// e^{i*ph} for a phase given in fp64: ph is reduced modulo 2*pi in fp64 (two-term
+// 2*pi split) before an fp32 sincos.  Returns (cos, sin).
+__device__ __forceinline__ float2 reduced_cis(double ph) {
   constexpr double kTwoPiHi = 6.283185307179586232;
   constexpr double kTwoPiLo = 2.449293598294706e-16;
   constexpr double kInvTwoPi = 0.15915494309189535;
-  const double ph = sc.omega[f] * (double)t;
   const double q = rint(ph * kInvTwoPi);
   double r = fma(-q, kTwoPiHi, ph);
   r = fma(-q, kTwoPiLo, r);
   float sn, cs;
   sincosf((float)r, &sn, &cs);
+  return make_float2(cs, sn);
+}
+
+__device__ __forceinline__ float2 step_phase(const StepConst &sc, int f, int t) {
+  const float2 e = reduced_cis(sc.omega[f] * (double)t);
   const float2 p = sc.phi[f];
-  return make_float2(cs * p.x - sn * p.y, cs * p.y + sn * p.x);
+  return make_float2(e.x * p.x - e.y * p.y, e.x * p.y + e.y * p.x);
 }
 
 // wts layout [G][3][F]: Re A, Im A, W for the G query heads of KV head g.

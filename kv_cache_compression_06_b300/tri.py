@@ -26,7 +26,10 @@ _COMPACT = {"ordered": TRI_COMPACT_ORDERED, "holefill": TRI_COMPACT_HOLEFILL}
 EXPORTED = ("tri_calibrate_stats", "tri_workspace_bytes", "tri_score", "tri_select_topb",
             "tri_compact_kv", "tri_compress_step", "tri_get_device_status",
             "tri_clear_device_status", "tri_status_string", "tri_version",
-            "tri_compress_step_static_scratch")
+            "tri_compress_step_static_scratch", "tri_calib_reset", "tri_calib_accumulate",
+            "tri_calib_merge", "tri_calib_finalize", "tri_distance_curves", "tri_check_bounded_wait",
+            "tri_append_kv", "tri_decode_workspace_bytes", "tri_decode_attention")
+TRI_CALIB_ACC_DOUBLES = 8
 
 
 class TriError(RuntimeError):
@@ -78,6 +81,15 @@ def lib() -> ctypes.CDLL:
             "tri_clear_device_status": [P],
             "tri_status_string": [I],
             "tri_version": [],
+            "tri_calib_reset": [P, I, I, I, P],
+            "tri_calib_accumulate": [P, I, I64, I, I, I, I, I64, I64, P, P],
+            "tri_calib_merge": [P, P, I, I, I, P],
+            "tri_calib_finalize": [P, I, I, I, P, P, P, P],
+            "tri_distance_curves": [P, P, P, P, I, I64, I, I, I, I, ctypes.c_double, I, I, P, P, P, P],
+            "tri_check_bounded_wait": [ctypes.c_uint32, P],
+            "tri_append_kv": [P, P, P, P, ctypes.c_double, I, P, P, P],
+            "tri_decode_workspace_bytes": [P, I, ctypes.POINTER(SZ)],
+            "tri_decode_attention": [P, P, I, P, ctypes.c_double, I, ctypes.c_float, P, P, SZ, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -216,6 +228,139 @@ def tri_calibrate_stats(q_pre: torch.Tensor, pairing: str = "half", out: Optiona
     return out
 
 
+def _pairing(pairing: str) -> int:
+    if pairing not in ("half", "interleaved"):
+        raise ValueError(pairing)
+    return TRI_PAIR_HALF if pairing == "half" else TRI_PAIR_INTERLEAVED
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return TRI_BF16
+    if t.dtype == torch.float32:
+        return TRI_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def calib_accumulator(L: int, H: int, d: int, device) -> torch.Tensor:
+    """A zeroed fp64 accumulator [L][H][d/2][TRI_CALIB_ACC_DOUBLES] for the
+    streamed calibration (allocated by torch; tri_calib_reset zeroes it on the GPU)."""
+    acc = torch.empty((L, H, d // 2, TRI_CALIB_ACC_DOUBLES), dtype=torch.float64, device=device)
+    tri_calib_reset(acc, stream=None)
+    return acc
+
+
+def tri_calib_reset(acc: torch.Tensor, stream=None) -> None:
+    L, H, F, _ = acc.shape
+    _check("tri_calib_reset", lib().tri_calib_reset(_ptr(acc), L, H, 2 * F, _stream(stream)))
+
+
+def tri_calib_accumulate(q: torch.Tensor, acc: torch.Tensor, pairing: str = "half", stream=None) -> None:
+    """Adds the samples of q to acc.  q is [L][n][H][d], or a strided view of
+    one (the sample and layer strides are passed through; the last two
+    dimensions must be contiguous), e.g. the query slice of a fused QKV
+    activation."""
+    L, n, H, d = q.shape
+    if q.stride(3) != 1 or q.stride(2) != d:
+        raise ValueError("the head and element dimensions of q must be contiguous")
+    if tuple(acc.shape) != (L, H, d // 2, TRI_CALIB_ACC_DOUBLES) or acc.dtype != torch.float64:
+        raise ValueError("acc does not match q")
+    st = lib().tri_calib_accumulate(_ptr(q), _dtype(q), n, L, H, d, _pairing(pairing), q.stride(1),
+                                    q.stride(0) if L > 1 else 0, _ptr(acc), _stream(stream))
+    _check("tri_calib_accumulate", st)
+
+
+def tri_calib_merge(acc: torch.Tensor, other: torch.Tensor, stream=None) -> None:
+    if acc.shape != other.shape:
+        raise ValueError("accumulators differ in shape")
+    L, H, F, _ = acc.shape
+    _check("tri_calib_merge", lib().tri_calib_merge(_ptr(acc), _ptr(other), L, H, 2 * F, _stream(stream)))
+
+
+def tri_calib_finalize(acc: torch.Tensor, out: Optional["Stats"] = None, stream=None) -> "Stats":
+    L, H, F, _ = acc.shape
+    if out is None:
+        dev = acc.device
+        out = Stats(torch.empty((L, H, F, 2), dtype=torch.float32, device=dev),
+                    torch.empty((L, H, F), dtype=torch.float32, device=dev),
+                    torch.empty((L, H, F), dtype=torch.float32, device=dev))
+    st = lib().tri_calib_finalize(_ptr(acc), L, H, 2 * F, _ptr(out.center), _ptr(out.R), _ptr(out.mag),
+                                  _stream(stream))
+    _check("tri_calib_finalize", st)
+    return out
+
+
+def tri_distance_curves(q_center: torch.Tensor, k_center: torch.Tensor, q_seq: Optional[torch.Tensor],
+                        k_seq: Optional[torch.Tensor], theta: float, n_delta: int, pairing: str = "half",
+                        stream=None):
+    """Distance-preference curves: (center_curve [L][Hq][n_delta], logit_curve
+    [L][Hq][n_delta] or None, corr [L][Hq] or None).  q_center [L][Hq][F][2],
+    k_center [L][Hkv][F][2]; q_seq [L][n][Hq][d], k_seq [L][n][Hkv][d] pre-RoPE
+    samples of one sequence (None: center curve only)."""
+    L, Hq, F, _ = q_center.shape
+    Hkv = k_center.shape[1]
+    d = 2 * F
+    dev = q_center.device
+    cc = torch.empty((L, Hq, n_delta), dtype=torch.float32, device=dev)
+    lc = corr = None
+    n, dt = 1, TRI_F32
+    if q_seq is not None:
+        q_seq, k_seq = q_seq.contiguous(), k_seq.contiguous()
+        n, dt = q_seq.shape[1], _dtype(q_seq)
+        lc = torch.empty_like(cc)
+        corr = torch.empty((L, Hq), dtype=torch.float32, device=dev)
+    st = lib().tri_distance_curves(_ptr(q_center.contiguous()), _ptr(k_center.contiguous()), _ptr(q_seq),
+                                   _ptr(k_seq), dt, n, L, Hq, Hkv, d, float(theta), _pairing(pairing),
+                                   int(n_delta), _ptr(cc), _ptr(lc), _ptr(corr), _stream(stream))
+    _check("tri_distance_curves", st)
+    return cc, lc, corr
+
+
+def tri_check_bounded_wait(limit_us: int = 1000, stream=None) -> None:
+    """Runs the bounded-wait health check (see include/tri.h): afterwards the
+    device status reads TRI_ERR_TIMEOUT until cleared."""
+    _check("tri_check_bounded_wait", lib().tri_check_bounded_wait(int(limit_us), _stream(stream)))
+
+
+def tri_append_kv(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, pos: torch.Tensor, theta: float,
+                  seq_len_out: torch.Tensor, pos_out: Optional[torch.Tensor] = None, pairing: str = "half",
+                  stream=None) -> None:
+    """Appends one token per unit: k_new, v_new [L][S][Hkv][d] (pre-RoPE key,
+    value) into slot seq_len[s]; seq_len_out = seq_len + 1, pos_out = pos + 1."""
+    c = cache.to_c()
+    st = lib().tri_append_kv(ctypes.byref(c), _ptr(k_new.contiguous()), _ptr(v_new.contiguous()), _ptr(pos),
+                             float(theta), _pairing(pairing), _ptr(seq_len_out), _ptr(pos_out), _stream(stream))
+    _check("tri_append_kv", st)
+
+
+def tri_decode_workspace_bytes(cache: KVCache, Hq: int) -> int:
+    c = cache.to_c()
+    n = ctypes.c_size_t(0)
+    _check("tri_decode_workspace_bytes", lib().tri_decode_workspace_bytes(ctypes.byref(c), int(Hq), ctypes.byref(n)))
+    return int(n.value)
+
+
+def tri_decode_attention(cache: KVCache, q: torch.Tensor, pos: torch.Tensor, theta: float,
+                         scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                         ws: Optional[torch.Tensor] = None, pairing: str = "half", stream=None) -> torch.Tensor:
+    """Single-query attention of q [L][S][Hq][d] (bf16, pre-RoPE, rotated to pos
+    inside) over every unit's cached keys; returns out [L][S][Hq][d] fp32."""
+    L, S, Hq, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((L, S, Hq, d), dtype=torch.float32, device=q.device)
+    if ws is None:
+        n = tri_decode_workspace_bytes(cache, Hq)
+        ws = None if n == 0 else torch.empty(n, dtype=torch.uint8, device=q.device)
+    c = cache.to_c()
+    st = lib().tri_decode_attention(ctypes.byref(c), _ptr(q.contiguous()), Hq, _ptr(pos), float(theta),
+                                    _pairing(pairing), float(scale), _ptr(out), _ptr(ws),
+                                    0 if ws is None else ws.numel(), _stream(stream))
+    _check("tri_decode_attention", st)
+    return out
+
+
 def tri_workspace_bytes(cache: KVCache, stats: Stats, params: Params) -> int:
     c, s = cache.to_c(), stats.to_c()
     p, _keep = params.to_c()
@@ -290,17 +435,19 @@ TRI_STATIC_SCRATCH_BYTES = 32 << 20
 
 def tri_compress_step_static_scratch(cache: KVCache, stats: Stats, params: Params,
                                      idx_out: Optional[torch.Tensor] = None,
-                                     new_len: Optional[torch.Tensor] = None, stream=None):
+                                     new_len: Optional[torch.Tensor] = None, stream=None,
+                                     compact: str = "ordered"):
     """tri_compress_step without a caller workspace, for callers that cannot
     allocate device memory (e.g. an engine that reserved all of it for its
     KV-cache pool).  Long units use the library's built-in scratch of
     TRI_STATIC_SCRATCH_BYTES bytes, shared by every call on the device: calls
     that overlap on the GPU race.  Make the first call on a device before any
-    stream capture (it looks up the scratch address)."""
+    stream capture (it looks up the scratch address).  compact = 'ordered' or
+    'holefill', as for tri_compress_step."""
     c, s = cache.to_c(), stats.to_c()
     p, _keep = params.to_c()
     st = lib().tri_compress_step_static_scratch(ctypes.byref(c), ctypes.byref(s), ctypes.byref(p),
-                                                TRI_COMPACT_ORDERED, _ptr(idx_out), _ptr(new_len),
+                                                _COMPACT[compact], _ptr(idx_out), _ptr(new_len),
                                                 _stream(stream))
     if st == TRI_ERR_WORKSPACE:
         need = tri_workspace_bytes(cache, stats, params)

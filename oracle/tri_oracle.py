@@ -49,6 +49,7 @@ Where the pages are silent or garbled, the readings taken here are:
 from __future__ import annotations
 
 import itertools
+import math
 from typing import Sequence
 
 import numpy as np
@@ -72,6 +73,33 @@ def to_bands(x: np.ndarray, pairing: str = "half") -> np.ndarray:
     if pairing == "interleaved":
         return x[..., 0::2] + 1j * x[..., 1::2]
     raise ValueError(pairing)
+
+
+# ----------------------------------------------------------------------------
+# RoPE as the model applies it (real 2x2 rotation of each band pair)  [W3-TRIG]
+# ----------------------------------------------------------------------------
+def rope(x: np.ndarray, pos, theta: float, pairing: str = "half") -> np.ndarray:
+    """Rotates x [..., d] to position pos (a scalar, or an array broadcasting
+    against x's leading dimensions): the pair (a, b) of band f becomes
+    (a*cos(w) - b*sin(w), a*sin(w) + b*cos(w)), w = omega_f * pos.  Written with
+    real rotations, independently of to_bands."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    F = d // 2
+    om = band_frequencies(d, theta)
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * om            # [..., F]
+    c, sn = np.cos(ang), np.sin(ang)
+    if pairing == "half":
+        ia, ib = np.arange(F), np.arange(F) + F
+    elif pairing == "interleaved":
+        ia, ib = 2 * np.arange(F), 2 * np.arange(F) + 1
+    else:
+        raise ValueError(pairing)
+    out = np.empty(np.broadcast_shapes(x.shape, ang.shape[:-1] + (d,)))
+    a, b = x[..., ia], x[..., ib]
+    out[..., ia] = a * c - b * sn
+    out[..., ib] = a * sn + b * c
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -220,15 +248,79 @@ def holefill_layout(kept: np.ndarray, B: int) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# Distance-preference curves  [W3-TRIG]
+# ----------------------------------------------------------------------------
+def center_curve(cq: np.ndarray, ck: np.ndarray, d: int, theta: float, n_delta: int) -> np.ndarray:
+    """The trigonometric series of one query head against its KV head, from the
+    centers: C(delta) = sum_f Re[cq_f * conj(ck_f) * e^{i*omega_f*delta}],
+    delta = 0..n_delta-1.  cq, ck: [F] complex."""
+    om = band_frequencies(d, theta)
+    delta = np.arange(n_delta, dtype=np.float64)
+    terms = cq[None, :] * np.conj(ck)[None, :] * np.exp(1j * om[None, :] * delta[:, None])
+    return np.real(terms).sum(axis=1)
+
+
+def logit_curve(q_seq: np.ndarray, k_seq: np.ndarray, theta: float, n_delta: int,
+                pairing: str = "half") -> np.ndarray:
+    """The exact mean RoPE logit at each distance over one sequence: query
+    sample j sits at position j, key sample i at position i, and
+    E(delta) = mean over i in [0, n - delta) of rope(q_{i+delta}, i+delta) . rope(k_i, i).
+    q_seq, k_seq: [n][d] pre-RoPE samples."""
+    n = q_seq.shape[0]
+    pos = np.arange(n, dtype=np.float64)
+    qr = rope(q_seq, pos, theta, pairing)
+    kr = rope(k_seq, pos, theta, pairing)
+    out = np.empty(n_delta)
+    for dl in range(n_delta):
+        out[dl] = np.mean(np.sum(qr[dl:] * kr[: n - dl], axis=1))
+    return out
+
+
+def pearson(a: np.ndarray, b: np.ndarray) -> float:
+    """Pearson correlation; 0 when either series is constant."""
+    a = np.asarray(a, dtype=np.float64) - np.mean(a)
+    b = np.asarray(b, dtype=np.float64) - np.mean(b)
+    den = math.sqrt(float(np.sum(a * a)) * float(np.sum(b * b)))
+    return float(np.sum(a * b)) / den if den > 0 else 0.0
+
+
+# ----------------------------------------------------------------------------
+# Decode attention over a (compressed) cache  [W3-TRIG] (the RoPE attention
+# logit), [W3-PRUNE] (online decoding with window pruning every 128 tokens)
+# ----------------------------------------------------------------------------
+def decode_attention(q_post: np.ndarray, k_post: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
+    """Softmax attention of the G post-RoPE query vectors q_post [G][d] of one
+    KV head over its N cached post-RoPE keys k_post [N][d] and values v [N][d]:
+    out[h] = sum_i w_{h,i} v_i with w_{h,i} proportional to exp(scale * q_h . k_i),
+    normalised over i.  fp64; the largest logit of each head is subtracted
+    before exp (the weights are unchanged)."""
+    q = np.asarray(q_post, dtype=np.float64)
+    k = np.asarray(k_post, dtype=np.float64)
+    logits = scale * (q @ k.T)                                        # [G][N]
+    e = np.exp(logits - logits.max(axis=1, keepdims=True))
+    w = e / e.sum(axis=1, keepdims=True)
+    return w @ np.asarray(v, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------
 # One unit (sequence, layer, KV head) end to end
 # ----------------------------------------------------------------------------
-def compress_unit(center, R, m, k_post, v, pos, t, offsets, theta, B, pairing="half"):
+def compress_unit(center, R, m, k_post, v, pos, t, offsets, theta, B, pairing="half", route="offsets"):
     """Score -> GQA aggregate -> top-B -> compact for one unit.
 
     center/R/m: [G][F] statistics of the G query heads of this KV head.
+    route: "offsets" scores with the per-offset trig score (keys un-rotated by
+    their positions `pos`); "closed" with trig_score_closed_form (the same
+    average through the per-band offset sum, positions not needed), which is
+    far cheaper for long units.
     Returns dict(s=[G][N], a=[N], idx=[min(N,B)], k=[min(N,B)][d], v=...).
     """
-    s = key_scores(center, R, m, k_post, pos, t, offsets, theta, pairing)
+    if route == "offsets":
+        s = key_scores(center, R, m, k_post, pos, t, offsets, theta, pairing)
+    elif route == "closed":
+        s = trig_score_closed_form(center, k_post, t, offsets, theta, pairing) + norm_score(R, m, k_post, pairing)
+    else:
+        raise ValueError(route)
     a = gqa_aggregate(s)
     idx = select_topb(a, B)
     out = {"s": s, "a": a, "idx": idx, "k": compact(k_post, idx), "v": compact(v, idx)}

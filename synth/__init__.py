@@ -10,5 +10,6 @@ from .generate import (  # noqa: F401
     generate_layer,
     unit_rows,
     seed_for,
+    sequence_samples,
     vonmises,
 )

@@ -258,6 +258,41 @@ def generate_layer(w: Workload, layer: int, device="cpu", with_q: bool = True):
     return out
 
 
+def _samples(gen, c_re, c_im, kappa, n, device, outlier_frac=0.0, outlier_scale=3.0):
+    """n samples per head around the centers [H][F]: center * e^{i*phi} * r,
+    phi ~ von Mises(0, kappa_h), r ~ N(1, 0.2) (optionally scaled outliers).
+    Returns (re, im) [n][H][F] float64."""
+    H, F = c_re.shape
+    kap = torch.as_tensor(kappa, dtype=torch.float64, device=device).view(1, H, 1)
+    phi = vonmises(kap, (n, H, F), gen)
+    r = 1.0 + 0.2 * torch.randn((n, H, F), generator=gen, device=device, dtype=torch.float64)
+    if outlier_frac > 0:
+        sel = torch.rand((n, H, 1), generator=gen, device=device, dtype=torch.float64) < outlier_frac
+        r = torch.where(sel, r * outlier_scale, r)
+    cs, sn = torch.cos(phi), torch.sin(phi)
+    return r * (c_re * cs - c_im * sn), r * (c_re * sn + c_im * cs)
+
+
+def sequence_samples(w: Workload, layer: int, n: int, device="cpu", kappa_q=None, kappa_k=None,
+                     tag: str = "seq"):
+    """Pre-RoPE samples of one sequence of n tokens for one layer: queries
+    q [n][Hq][d], keys k [n][Hkv][d] and values v [n][Hkv][d] (float64), drawn
+    with the recipe above from centers of their own seed (name, tag, layer).
+    kappa_q / kappa_k override the per-head concentration (a scalar or one
+    value per head).  Token i sits at position i; nothing here is rotated."""
+    device = torch.device(device)
+    g = _gen(device, w.name, tag, layer)
+    qc = _centers(g, (w.Hq, w.F), device)
+    kc = _centers(g, (w.Hkv, w.F), device)
+    kq = head_kappas(w, layer, "q", w.Hq) if kappa_q is None else np.broadcast_to(kappa_q, (w.Hq,))
+    kk = head_kappas(w, layer, "k", w.Hkv) if kappa_k is None else np.broadcast_to(kappa_k, (w.Hkv,))
+    q = _bands_to_vec(*_samples(g, qc[0], qc[1], np.array(kq, dtype=np.float64), n, device), w.pairing)
+    k = _bands_to_vec(*_samples(g, kc[0], kc[1], np.array(kk, dtype=np.float64), n, device,
+                                w.outlier_frac, w.outlier_scale), w.pairing)
+    v = torch.randn((n, w.Hkv, w.d), generator=g, device=device, dtype=torch.float64)
+    return q, k, v
+
+
 def block_table(w: Workload, device="cpu"):
     """Random block table for a paged workload: [S][max_blocks] int32 (unused = 0),
     plus the number of physical blocks per layer pool."""

@@ -39,7 +39,7 @@ def _check_stats(stats, ref, li):
     np.testing.assert_allclose(stats.mag[li].double().cpu().numpy(), m, rtol=1e-4)
 
 
-def run_and_check(w, data, units, dev, unfused=True):
+def run_and_check(w, data, units, dev, unfused=True, route="offsets"):
     """Runs every entry point on the whole workload and checks `units`
     (list of (layer index, sequence, KV head)).  Returns the number of kept-set
     differences that fell inside the tie band."""
@@ -77,7 +77,7 @@ def run_and_check(w, data, units, dev, unfused=True):
         kr, vr = pristine[(li, s, g)]
         N = kr.shape[0]
         t = int(data["t"][s])
-        ref = H.oracle_unit(w, ostats[li], kr, vr, g, t)
+        ref = H.oracle_unit(w, ostats[li], kr, vr, g, t, route=route)
         H.check_scores(raw[li, s, g * w.G:(g + 1) * w.G, :N].cpu().numpy(), ref["s"])
         H.check_agg(agg[li, s, g, :N].cpu().numpy(), ref["a"])
         gi = idx[li, s, g].cpu().numpy()

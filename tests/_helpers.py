@@ -20,13 +20,15 @@ def unit_stats(center_all, R_all, m_all, g, G):
     return center_all[sl], R_all[sl], m_all[sl]
 
 
-def oracle_unit(w, stats_l, k_rows, v_rows, g, t):
+def oracle_unit(w, stats_l, k_rows, v_rows, g, t, route="offsets"):
     """Runs the oracle on one unit.  stats_l = oracle (center, R, m) of the layer;
-    k_rows/v_rows [N][d] float64 in logical slot order, positions 0..N-1."""
+    k_rows/v_rows [N][d] float64 in logical slot order, positions 0..N-1.
+    route: the oracle's per-offset route, or its closed form ("closed", pinned
+    equal to it) for the many long units of the large workloads."""
     c, R, m = unit_stats(*stats_l, g, w.G)
     N = k_rows.shape[0]
     return O.compress_unit(c, R, m, k_rows, v_rows, np.arange(N, dtype=np.float64), t,
-                           list(w.offsets), w.theta, w.budget, w.pairing)
+                           list(w.offsets), w.theta, w.budget, w.pairing, route=route)
 
 
 def check_scores(s_gpu, s_ref):

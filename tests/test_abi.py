@@ -145,3 +145,56 @@ def test_workspace_query_is_host_only():
     assert L.tri_workspace_bytes(ctypes.byref(c), ctypes.byref(s), ctypes.byref(p), ctypes.byref(n)) == 0
     units, G, ntiles = 2 * 3 * 8, 4, 16
     assert n.value >= units * G * 32768 * 4 + units * ntiles * G * 8
+
+
+def test_streamed_calibration_rejects_bad_arguments():
+    L = T.lib()
+    # reset / merge / finalize: shapes and pointers
+    assert L.tri_calib_reset(None, 1, 2, 64, None) == T.TRI_ERR_INVALID
+    assert L.tri_calib_reset(FAKE + 4, 1, 2, 64, None) == T.TRI_ERR_INVALID        # not 8-byte aligned
+    assert L.tri_calib_reset(FAKE, 0, 2, 64, None) == T.TRI_ERR_INVALID
+    assert L.tri_calib_reset(FAKE, 1, 2, 96, None) == T.TRI_ERR_INVALID
+    assert L.tri_calib_merge(FAKE, FAKE, 1, 2, 64, None) == T.TRI_ERR_INVALID      # acc aliases other
+    assert L.tri_calib_merge(FAKE, None, 1, 2, 64, None) == T.TRI_ERR_INVALID
+    assert L.tri_calib_finalize(FAKE, 1, 2, 64, FAKE, None, FAKE, None) == T.TRI_ERR_INVALID
+    # accumulate: q alignment, dtype, pairing, strides
+    acc = FAKE
+    args = dict(q=FAKE, dt=T.TRI_BF16, n=10, L=1, H=2, d=64, pr=0, ss=0, ls=0)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return L.tri_calib_accumulate(a["q"], a["dt"], a["n"], a["L"], a["H"], a["d"], a["pr"], a["ss"], a["ls"],
+                                      acc, None)
+
+    assert call(q=None) == T.TRI_ERR_INVALID
+    assert call(q=FAKE + 8) == T.TRI_ERR_INVALID          # q must be 16-byte aligned
+    assert call(dt=5) == T.TRI_ERR_INVALID
+    assert call(pr=3) == T.TRI_ERR_INVALID
+    assert call(n=-1) == T.TRI_ERR_INVALID
+    assert call(ss=100) == T.TRI_ERR_INVALID              # < H*d
+    assert call(ss=130) == T.TRI_ERR_INVALID              # not a multiple of 4 elements
+    assert call(L=2, ls=6) == T.TRI_ERR_INVALID
+    assert call(n=0) == T.TRI_OK                          # nothing to add: returns before any launch
+    assert call(n=0, q=None) == T.TRI_OK                  # and reads nothing
+
+
+def test_distance_curves_reject_bad_arguments():
+    L = T.lib()
+
+    def call(Hq=4, Hkv=2, d=64, theta=1e4, n=100, nd=50, q=FAKE, k=FAKE, lc=FAKE, corr=FAKE, dt=0, pr=0):
+        return L.tri_distance_curves(FAKE, FAKE, q, k, dt, n, 1, Hq, Hkv, d, theta, pr, nd, FAKE, lc, corr, None)
+
+    assert call(Hq=6, Hkv=4) == T.TRI_ERR_INVALID
+    assert call(d=48) == T.TRI_ERR_INVALID
+    assert call(theta=-1.0) == T.TRI_ERR_INVALID
+    assert call(nd=0) == T.TRI_ERR_INVALID
+    assert call(nd=101) == T.TRI_ERR_INVALID              # more distances than samples
+    assert call(q=None) == T.TRI_ERR_INVALID              # logit curve asked for without samples
+    assert call(lc=None) == T.TRI_ERR_INVALID             # corr needs the logit curve
+    assert call(dt=9) == T.TRI_ERR_INVALID
+    assert call(pr=2) == T.TRI_ERR_INVALID
+
+
+def test_bounded_wait_check_rejects_bad_limits():
+    assert T.lib().tri_check_bounded_wait(0, None) == T.TRI_ERR_INVALID
+    assert T.lib().tri_check_bounded_wait(1000001, None) == T.TRI_ERR_INVALID

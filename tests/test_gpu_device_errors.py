@@ -95,3 +95,38 @@ def test_seq_len_beyond_cap_is_reported():
     assert torch.equal(cache.k[0, 1], k_before[0, 1])
     assert not torch.equal(cache.k[0, 0], k_before[0, 0])
     tk.tri_clear_device_status()
+
+
+@pytest.mark.parametrize("n_keys,budget", [(900, 500), (12000, 1024)], ids=["fused", "long"])
+def test_bounded_wait_gives_up_and_later_calls_return_without_work(n_keys, budget):
+    """tri_check_bounded_wait waits (1 ms limit) on a barrier nothing arrives at,
+    with nothing in flight: the wait gives up and records TRI_ERR_TIMEOUT.  The
+    next tri_compress_step then returns without touching the cache, idx or the
+    new lengths; once the status is cleared the same call runs normally."""
+    w = Workload(name=f"wait_check_{n_keys}", L=1, S=2, Hq=8, Hkv=2, d=128, theta=1e6, dtype="bf16",
+                 budget=budget, offsets=GEO16, n_keys=n_keys)
+    data = generate(w, device=DEV)
+    ref = _reference_idx(w, data)
+    cache, stats, params = C.setup(w, data, DEV)
+    ws = tk.workspace(cache, stats, params)
+    k0, v0 = cache.k.clone(), cache.v.clone()
+    idx = torch.full((1, w.S, w.Hkv, w.budget), -7, dtype=torch.int32, device=DEV)
+    new_len = torch.full((w.S,), -7, dtype=torch.int32, device=DEV)
+    try:
+        tk.tri_clear_device_status()
+        T.tri_check_bounded_wait(1000)
+        torch.cuda.synchronize()
+        assert tk.tri_get_device_status() == T.TRI_ERR_TIMEOUT
+        tk.tri_compress_step(cache, stats, params, idx_out=idx, new_len=new_len, ws=ws)
+        torch.cuda.synchronize()
+        assert tk.tri_get_device_status() == T.TRI_ERR_TIMEOUT
+        assert torch.equal(cache.k, k0) and torch.equal(cache.v, v0)
+        assert torch.all(idx == -7) and torch.all(new_len == -7)
+    finally:
+        tk.tri_clear_device_status()
+    assert tk.tri_get_device_status() == T.TRI_OK
+    tk.tri_compress_step(cache, stats, params, idx_out=idx, new_len=new_len, ws=ws)
+    torch.cuda.synchronize()
+    assert tk.tri_get_device_status() == T.TRI_OK
+    assert torch.equal(idx, ref)
+    assert new_len.tolist() == [budget] * w.S

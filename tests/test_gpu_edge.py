@@ -18,6 +18,9 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 GEO16 = tuple(2 ** i for i in range(17))
 GEO10 = tuple(2 ** i for i in range(11))
+# the linear offset set of the offset ablation (results section of the method's
+# write-up: geometric sampling beats linear), o = 64 k, k = 1..32
+LIN32 = tuple(64 * k for k in range(1, 33))
 
 
 def W(name, **kw):
@@ -42,6 +45,10 @@ CASES = [
     W("edge_long_mma_g8_paged32", Hq=16, n_range=(12000, 16000), budget=1024, paged=True, block=32),
     W("edge_long_cuda_f32_g2", Hq=4, d=64, dtype="f32", n_range=(30000, 40000), budget=2048, S=2),
     W("edge_long_cuda_inter_g4", Hq=8, pairing="interleaved", n_range=(11000, 14000), budget=1024),
+    # linear future offsets instead of geometric ones
+    W("edge_linear_offsets_fused_g4", Hq=8, n_range=(600, 1800), budget=700, offsets=LIN32),
+    W("edge_linear_offsets_long_g4", Hq=8, n_range=(9000, 13000), budget=1024, offsets=LIN32),
+    W("edge_linear_offsets_long_g8_paged", Hq=16, n_range=(12000, 16000), budget=1024, paged=True, offsets=LIN32),
 ]
 
 

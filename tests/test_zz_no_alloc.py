@@ -7,7 +7,8 @@ array built into it instead.
 The GPU test runs two calls in a row (the second one sees the first one's
 leftovers in the shared scratch) on long, ragged units that take the
 scratch-using path, and checks each against tri_compress_step with a caller
-workspace: kept indices, new lengths and compacted K/V must be identical.
+workspace: kept indices, new lengths and compacted K/V must be identical, for
+both compaction layouts (ordered and hole-fill).
 This file is named to be collected last.
 """
 import ctypes
@@ -58,7 +59,8 @@ def _setup(w, dev):
 
 
 @pytest.mark.gpu
-def test_static_scratch_matches_workspace_entry_point_twice_in_a_row():
+@pytest.mark.parametrize("compact", ["ordered", "holefill"])
+def test_static_scratch_matches_workspace_entry_point_twice_in_a_row(compact):
     dev = torch.device("cuda:0")
     for w in CASES:
         cache, stats, params = _setup(w, dev)
@@ -71,7 +73,7 @@ def test_static_scratch_matches_workspace_entry_point_twice_in_a_row():
         ws = tk.workspace(cache, stats, params)
         idx_ref = torch.full(shape, -7, dtype=torch.int32, device=dev)
         len_ref = torch.full((cache.S,), -7, dtype=torch.int32, device=dev)
-        tk.tri_compress_step(cache, stats, params, idx_out=idx_ref, new_len=len_ref, ws=ws)
+        tk.tri_compress_step(cache, stats, params, idx_out=idx_ref, new_len=len_ref, ws=ws, compact=compact)
         torch.cuda.synchronize()
         assert tk.tri_get_device_status() == 0
         k_ref, v_ref = cache.k.clone(), cache.v.clone()
@@ -81,7 +83,7 @@ def test_static_scratch_matches_workspace_entry_point_twice_in_a_row():
         cache.v.copy_(v0)
         idx = torch.full(shape, -7, dtype=torch.int32, device=dev)
         new_len = torch.full((cache.S,), -7, dtype=torch.int32, device=dev)
-        tk.tri_compress_step_static_scratch(cache, stats, params, idx_out=idx, new_len=new_len)
+        tk.tri_compress_step_static_scratch(cache, stats, params, idx_out=idx, new_len=new_len, compact=compact)
         torch.cuda.synchronize()
         assert tk.tri_get_device_status() == 0
 
