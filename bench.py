@@ -7,10 +7,16 @@ GQA z/max, top-B, in-place compaction of K and V), with inputs resident in HBM.
 The compaction is in place, so the cache is restored from a pristine copy
 before every step (untimed; the 5.1 GB copy also flushes the 126 MB L2).
 
+The same run also times, each in its own timed region with its own clock
+record and algorithmic bytes ("extras"): the hole-fill layout on the same
+workload, the long 32k-key workload (36 layers x 4 sequences) and a layer group
+of the paged Qwen3-32B-shaped workload (its 64 layers do not fit HBM).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
 
-Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle on a
-bounded sample of the same workload.
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+(closed-form route, one process per host core) on a bounded sample of the same
+workload.
 """
 import argparse
 import json
@@ -20,9 +26,11 @@ import subprocess
 import sys
 import time
 
-# The CPU-oracle leg runs single-threaded: pin numpy's BLAS pool before import.
+# The CPU-oracle leg runs one worker process per host core, each with one BLAS
+# thread (set before numpy is imported; spawned workers inherit it).
 os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
 os.environ.setdefault("MKL_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
 
 import numpy as np  # noqa: E402
 
@@ -53,61 +61,103 @@ def _config(w, extra=None):
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def oracle_layer(w):
-    """Layer 0 of the workload on the CPU with the oracle's statistics (untimed)."""
+_ORACLE_STATE = {}
+
+
+def _oracle_worker_init(w):
+    """Pool initialiser: layer 0 of the workload on the CPU and the oracle's
+    statistics for it (untimed; every worker builds its own copy)."""
     from oracle import tri_oracle as O
     from synth import generate_layer
 
     lay = generate_layer(w, 0, "cpu", with_q=True)
-    return lay, O.calibrate(lay["q_pre"].double().numpy(), w.pairing)
+    _ORACLE_STATE["w"] = w
+    _ORACLE_STATE["layer"] = lay
+    _ORACLE_STATE["stats"] = O.calibrate(lay["q_pre"].double().numpy(), w.pairing)
 
 
-def oracle_sample(w, budget_s, max_units=None, seed=0, layer=None):
-    """Runs the fp64 oracle on sampled units of layer 0 (generated on the CPU,
-    or the given oracle_layer) until budget_s seconds of CPU work; returns
-    (keys, seconds, units, threads)."""
+def _oracle_unit(unit):
+    """One unit (sequence s, KV head g of layer 0) through the oracle's
+    closed-form route: closed-form trig score + norm score, GQA z/max, top-B,
+    ordered compaction of K and V.  Returns the unit's key count."""
     from oracle import tri_oracle as O
 
-    lay, stats = layer if layer is not None else oracle_layer(w)
-    rng = np.random.default_rng(seed)
-    keys = units = 0
-    t0 = time.perf_counter()
-    while True:
-        s, g = int(rng.integers(w.S)), int(rng.integers(w.Hkv))
-        n = lay["seq_len"][s]
-        kr = lay["k"][s, g, :n].double().numpy()
-        vr = lay["v"][s, g, :n].double().numpy()
-        sl = slice(g * w.G, (g + 1) * w.G)
-        O.compress_unit(stats[0][sl], stats[1][sl], stats[2][sl], kr, vr, np.arange(n, dtype=np.float64),
-                        n, list(w.offsets), w.theta, w.budget, w.pairing)
-        keys += n
-        units += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or (max_units and units >= max_units):
-            return keys, el, units, 1
+    s, g = unit
+    w, lay, (c, R, m) = _ORACLE_STATE["w"], _ORACLE_STATE["layer"], _ORACLE_STATE["stats"]
+    n = lay["seq_len"][s]
+    kr = lay["k"][s, g, :n].double().numpy()
+    vr = lay["v"][s, g, :n].double().numpy()
+    sl = slice(g * w.G, (g + 1) * w.G)
+    sc = O.trig_score_closed_form(c[sl], kr, n, list(w.offsets), w.theta, w.pairing) + O.norm_score(
+        R[sl], m[sl], kr, w.pairing)
+    idx = O.select_topb(O.gqa_aggregate(sc), w.budget)
+    O.compact(kr, idx)
+    O.compact(vr, idx)
+    return n
+
+
+class OraclePool:
+    """The oracle on every host core: one spawned worker process per core (a
+    fresh interpreter, started before any GPU work), each with one BLAS thread."""
+
+    def __init__(self, w, cores=None):
+        import multiprocessing as mp
+        self.w = w
+        self.cores = cores or os.cpu_count() or 1
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_worker_init, initargs=(w,))
+        self.rng = np.random.default_rng(0)
+        self.pool.map(_oracle_unit, self._units(self.cores))     # every worker has its layer
+
+    def _units(self, k):
+        return [(int(self.rng.integers(self.w.S)), int(self.rng.integers(self.w.Hkv))) for _ in range(k)]
+
+    def run(self, n_units):
+        """Runs n_units random units of layer 0; returns (keys, seconds)."""
+        units = self._units(n_units)
+        t0 = time.perf_counter()
+        keys = sum(self.pool.map(_oracle_unit, units, chunksize=1))
+        return keys, time.perf_counter() - t0
+
+    def run_for(self, budget_s):
+        """Batches of 4 units per core until budget_s seconds; returns (keys, seconds, units)."""
+        keys = units = 0
+        el = 0.0
+        while el < budget_s:
+            k, t = self.run(4 * self.cores)
+            keys, el, units = keys + k, el + t, units + 4 * self.cores
+        return keys, el, units
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def _world():
+    return int(os.environ.get("WORLD_SIZE", "1"))
 
 
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    per_step = []
-    total_keys = 0
-    layer = oracle_layer(w)
+    pool = OraclePool(w)
+    per_step, total_keys = [], 0
     for i in range(args.warmup + args.steps):
-        keys, el, units, cores = oracle_sample(w, 0.0, max_units=2, seed=1000 + i, layer=layer)
+        keys, el = pool.run(2 * pool.cores)
         if i >= args.warmup:
             per_step.append(el)
             total_keys += keys
+    pool.close()
     T = sum(per_step)
     value = total_keys / T
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": args.gpus,
+    sample = (f"per step: {2 * pool.cores} random units (seq, KV head) of layer 0 (N={w.n_keys or 'ragged'} keys each), "
+              f"closed-form route, fp64 numpy, {pool.cores} worker processes x 1 thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": _world(),
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * T / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": _config(w, {"sample": "2 units (seq, KV head) of layer 0 per step"}),
-            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": cores, "kind": "oracle",
-                             "sample": "per step: 2 random units of layer 0 (N=2176 keys each), "
-                                       "per-offset route, fp64 numpy, 1 thread"},
+            "data": "synthetic", "config": _config(w, {"sample": sample}),
+            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": pool.cores, "kind": "oracle",
+                             "route": "closed form", "sample": sample},
             "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -125,7 +175,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                       "--format=csv,noheader,nounits", "-lms", "20"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.p = None
@@ -194,7 +244,8 @@ def _select_kernel_name(w, cap, compact):
 def kernel_src_hash():
     import hashlib
     h = hashlib.sha1()
-    for f in ("tri.cu", "tri_path.cuh", "tri_device.cuh", "tri_mma.cuh"):
+    from kv_cache_compression_06_b300.build import CSRC
+    for f in CSRC:
         with open(os.path.join(ROOT, "kv_cache_compression_06_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -300,141 +351,311 @@ def run_e2e(tk, cache, stats, params, k0, v0, idx, new_len, steps, compact):
     return t, h2d, d2h
 
 
+def _kernel_name(w, cap, compact, launches):
+    mma = w.dtype == "bf16" and w.pairing == "half"
+    if launches == 1:
+        return f"fused_mma_kernel<{w.d},{w.G}>" if mma else f"fused_kernel<{w.d},{w.G},{w.dtype}>"
+    return ("phase_kernel+" + ("score_tiles_mma_kernel" if mma else "score_tiles_kernel") + "+"
+            + _select_kernel_name(w, cap, compact))
+
+
+class Measured:
+    """One workload on the GPU: generated, calibrated, restorable, timed."""
+
+    def __init__(self, tk, w, dev):
+        import torch
+        from synth import generate
+        self.tk, self.w, self.dev = tk, w, dev
+        self.data = generate(w, device=dev)
+        d = self.data
+        self.cache = tk.KVCache(d["k"], d["v"], d["seq_len"], Hkv=w.Hkv, block_table=d.get("block_table"),
+                                block=w.block)
+        self.stats = tk.tri_calibrate_stats(d["q_pre"], pairing=w.pairing)
+        d["q_pre"] = None
+        self.params = tk.Params(w.theta, d["t"], w.offsets, w.budget, pairing=w.pairing)
+        self.ws = tk.workspace(self.cache, self.stats, self.params)
+        self.launches = 1 if self.ws is None else 3   # fused kernel, or phases + score tiles + select/compact
+        self.k0, self.v0 = self.cache.k.clone(), self.cache.v.clone()
+        self.L = self.cache.L
+        self.idx = torch.empty((self.L, w.S, w.Hkv, w.budget), dtype=torch.int32, device=dev)
+        self.new_len = torch.empty(w.S, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+        # A cache smaller than L2 (126 MB) would stay resident across steps: write
+        # a 256 MB buffer after each restore so every step starts from a cold L2.
+        self.cache_bytes = 2 * self.k0.numel() * self.k0.element_size()
+        self.flush = (torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+                      if self.cache_bytes < (512 << 20) else None)
+
+    def restore(self):
+        self.cache.k.copy_(self.k0)
+        self.cache.v.copy_(self.v0)
+        if self.flush is not None:
+            self.flush.fill_(1)
+
+    def step(self, compact):
+        self.tk.tri_compress_step(self.cache, self.stats, self.params, idx_out=self.idx, new_len=self.new_len,
+                                  ws=self.ws, stream=self.stream, compact=compact)
+
+    def time(self, compact, steps, warmup, world, local, min_region_s=0.0):
+        """Mean seconds per step (max over ranks), per-step ms, clock summary.
+        With min_region_s > 0 the step count grows until the timed region
+        (restores included) lasts about that long, so that the clock sampler
+        sees it."""
+        import torch
+        import torch.distributed as dist
+        for _ in range(warmup):
+            self.restore()
+            self.step(compact)
+        torch.cuda.synchronize()
+        assert self.tk.tri_get_device_status() == 0
+        if min_region_s > 0:
+            t0 = time.perf_counter()
+            self.restore()
+            self.step(compact)
+            torch.cuda.synchronize()
+            steps = max(steps, int(math.ceil(min_region_s / max(time.perf_counter() - t0, 1e-6))))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            torch.cuda.nvtx.range_push("timed")
+            for i in range(steps):
+                self.restore()
+                ev[i][0].record(self.stream)
+                self.step(compact)
+                ev[i][1].record(self.stream)
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_pop()
+        if world > 1:
+            dist.barrier()
+        ms = [a.elapsed_time(b) for a, b in ev]
+        t_step = max_over_ranks(sum(ms) / len(ms) / 1e3, self.dev)
+        assert self.tk.tri_get_device_status() == 0
+        return t_step, ms, clk.summary()
+
+    def bytes(self, compact):
+        """Algorithmic bytes of the last step: K read for scoring + K/V moved
+        (read + write) by compaction, over the units the step compresses (N > B)."""
+        w = self.w
+        B, rb = w.budget, w.d * w.esize
+        lens = [int(x) for x in self.data["seq_len"].tolist()]
+        M = (_moved_rows(self.idx, self.data["seq_len"], B) if compact == "ordered"
+             else _moved_rows_holefill(self.idx, self.data["seq_len"], B))
+        scored = self.L * w.Hkv * sum(n for n in lens if n > B)
+        units_c = self.L * w.Hkv * sum(1 for n in lens if n > B)
+        return {"alg_bytes": scored * rb + 4 * M * rb, "alg_bytes_all_B": scored * rb + 4 * units_c * B * rb,
+                "moved_rows": M, "moved_rows_if_all_B": units_c * B, "units": self.L * w.S * w.Hkv,
+                "units_compressed": units_c, "n_keys": self.L * w.Hkv * sum(lens)}
+
+    def free(self):
+        for a in ("data", "cache", "stats", "params", "ws", "k0", "v0", "idx", "new_len", "flush"):
+            setattr(self, a, None)
+        import torch
+        torch.cuda.empty_cache()
+
+
+def _extra(m, compact, steps, warmup, world, local, peak, note):
+    """A workload timed in its own region: throughput, roofline fraction,
+    algorithmic bytes and its own clock record."""
+    t, ms, clocks = m.time(compact, steps, warmup, world, local, min_region_s=0.3)
+    steps = len(ms)
+    b = m.bytes(compact)
+    ach = b["alg_bytes"] / t / 1e9
+    l2 = (f"cache restored from a pristine {m.cache_bytes / 1e9:.3f} GB copy before every step"
+          + (" plus a 256 MB L2 flush" if m.flush is not None else " (flushes L2)") + "; untimed")
+    return {"config": _config(m.w, {"layers": m.L, "compaction": compact, "note": note, "l2": l2}),
+            "value": job_throughput(world, b["n_keys"], t), "unit": "keys/s", "ms_per_step": t * 1e3,
+            "steps": steps, "warmup": warmup, "step_ms_min": min(ms), "step_ms_median": float(np.median(ms)),
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                         "algorithmic_bytes_per_launch": b["alg_bytes"],
+                         "algorithmic_bytes_if_all_B_moved": b["alg_bytes_all_B"],
+                         "kernel": _kernel_name(m.w, m.cache.cap, compact, m.launches)},
+            "moved_rows": b["moved_rows"], "units_compressed": b["units_compressed"],
+            "gpu_launches": m.launches * steps, "clocks": clocks}
+
+
+def decode_leg(tk, dev, windows, warmup_windows, world, local, peak):
+    """The decode loop around the step on Qwen3-8B shapes (36 layers, 32/8 heads,
+    d = 128, bf16, 16 sequences, paged 16-token blocks, B = 2048): every token
+    appends K/V to all units and attends (tri_append_kv + tri_decode_attention
+    over all 36 layers at once), every 128 tokens tri_compress_step runs.  The
+    caches start at N = B, so each window grows them to 2176 and the step brings
+    them back to 2048 (the steady state of the benchmark workload).  Times the
+    decode tokens and the step of each window with CUDA events; the overhead is
+    the step's time over the window's decode time."""
+    import torch
+    from synth import WORKLOADS, generate
+    w = WORKLOADS[WORKLOAD].with_(name="decode_loop_qwen3_8b_36l_b16_paged", paged=True, block=16)
+    window, B = 128, w.budget
+    data = generate(w, device=dev)                       # 2176 rows per sequence
+    cache = tk.KVCache(data["k"], data["v"], torch.full((w.S,), B, dtype=torch.int32, device=dev), Hkv=w.Hkv,
+                       block_table=data["block_table"], block=w.block)
+    stats = tk.tri_calibrate_stats(data["q_pre"], pairing=w.pairing)
+    data["q_pre"] = None
+    pos = torch.full((w.S,), B, dtype=torch.int32, device=dev)
+    loop = tk.DecodeLoop(cache, stats, w.theta, w.offsets, B, pos, window=window)
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    qs = torch.randn((window, w.L, w.S, w.Hq, w.d), generator=g, device=dev).to(torch.bfloat16)
+    ks = torch.randn((window, w.L, w.S, w.Hkv, w.d), generator=g, device=dev).to(torch.bfloat16)
+    vs = torch.randn((window, w.L, w.S, w.Hkv, w.d), generator=g, device=dev).to(torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    loop.stream = stream
+
+    def run_window(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        for i in range(window):
+            loop.append(ks[i], vs[i])
+            loop.attend(qs[i])
+            trigger = loop.advance()
+        if evs is not None:
+            evs[1].record(stream)
+        assert trigger
+        loop.compress()
+        if evs is not None:
+            evs[2].record(stream)
+
+    for _ in range(warmup_windows):
+        run_window()
+    torch.cuda.synchronize()
+    assert tk.tri_get_device_status() == 0
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(windows)]
+    with ClockSampler(local) as clk:
+        for e in evs:
+            run_window(e)
+        torch.cuda.synchronize()
+    assert tk.tri_get_device_status() == 0
+    dec_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    cmp_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    d_tok = sum(dec_ms) / len(dec_ms) / window
+    d_cmp = sum(cmp_ms) / len(cmp_ms)
+    rb = w.d * w.esize
+    units = w.L * w.S * w.Hkv
+    # decode-step bytes: every unit reads its N K and V rows (N = 2049..2176 over
+    # the window, mean 2112.5) and writes one K and one V row
+    dec_bytes = units * (2 * rb * (B + (window + 1) / 2.0) + 2 * rb)
+    M = _moved_rows(loop.idx, torch.full((w.S,), B + window, dtype=torch.int32, device=dev), B)
+    cmp_bytes = units * (B + window) * rb + 4 * M * rb
+    d_ach = dec_bytes / (d_tok * 1e-3) / 1e9
+    c_ach = cmp_bytes / (d_cmp * 1e-3) / 1e9
+    res = {"config": {"workload": w.name, "layers": w.L, "batch": w.S, "q_heads": w.Hq, "kv_heads": w.Hkv,
+                      "head_dim": w.d, "budget": B, "window": window, "paged_block": w.block,
+                      "start_len": B, "note": "steady state: each window grows N from 2048 to 2176, the step "
+                                              "compresses back to 2048; inputs resident in HBM"},
+           "windows": windows, "warmup_windows": warmup_windows,
+           "decode_ms_per_token": d_tok, "compress_ms_per_trigger": d_cmp,
+           "overhead_frac": d_cmp / (window * d_tok),
+           "tokens_per_s": w.S * window / ((window * d_tok + d_cmp) * 1e-3),
+           "decode_roofline": {"bound": "hbm", "achieved": d_ach, "peak": peak, "unit": "GB/s",
+                               "frac": d_ach / peak, "algorithmic_bytes_per_token": dec_bytes,
+                               "kernels": "append_kv_kernel + decode_attn_kernel<128,4>"},
+           "compress_roofline": {"bound": "hbm", "achieved": c_ach, "peak": peak, "unit": "GB/s",
+                                 "frac": c_ach / peak, "algorithmic_bytes_per_launch": cmp_bytes},
+           "gpu_launches": windows * (2 * window + (1 if loop.cmp_ws is None else 3)),
+           "clocks": clk.summary()}
+    del loop, cache, stats, data, qs, ks, vs
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_b300(args, w):
     import torch
     import torch.distributed as dist
 
     import kv_cache_compression_06_b300 as tk
-    from synth import generate
+    from synth import WORKLOADS
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+    world = _world()
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    # CPU oracle baseline first (rank 0, N=1), before any GPU work.
+    # CPU oracle baseline first (rank 0, N=1), before any GPU work: the worker
+    # processes are spawned, not forked from a CUDA process.
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and w.name == WORKLOAD:
-        keys, el, units, cores = oracle_sample(w, args.cpu_seconds)
-        cpu = {"value": keys / el, "unit": "keys/s", "cores": cores, "kind": "oracle",
-               "sample": f"{units} random units (seq, KV head) of layer 0, {keys} keys in all, "
-                         f"{el:.1f} s; per-offset route, fp64 numpy, 1 thread"}
+        pool = OraclePool(w)
+        keys, el, units = pool.run_for(args.cpu_seconds)
+        pool.close()
+        cpu = {"value": keys / el, "unit": "keys/s", "cores": pool.cores, "kind": "oracle", "route": "closed form",
+               "sample": f"{units} random units (seq, KV head) of layer 0, {keys} keys in all, {el:.1f} s wall on "
+                         f"{pool.cores} worker processes (os.cpu_count()) x 1 BLAS thread; closed-form route, "
+                         f"fp64 numpy"}
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    data = generate(w, device=dev)
-    cache = tk.KVCache(data["k"], data["v"], data["seq_len"], Hkv=w.Hkv,
-                       block_table=data.get("block_table"), block=w.block)
-    stats = tk.tri_calibrate_stats(data["q_pre"], pairing=w.pairing)
-    del data["q_pre"]
-    params = tk.Params(w.theta, data["t"], w.offsets, w.budget, pairing=w.pairing)
-    ws = tk.workspace(cache, stats, params)
-    launches = 1 if ws is None else 3   # fused kernel, or phases + score tiles + select/compact
-    k0, v0 = cache.k.clone(), cache.v.clone()
-    L = cache.L
-    idx = torch.empty((L, w.S, w.Hkv, w.budget), dtype=torch.int32, device=dev)
-    new_len = torch.empty(w.S, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
+    peak, peak_kind = _peaks()
 
-    # A cache smaller than L2 (126 MB) would stay resident across steps: write a
-    # 256 MB buffer after each restore so every step starts from a cold L2.
-    cache_bytes = 2 * k0.numel() * k0.element_size()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if cache_bytes < (512 << 20) else None
-
-    def restore():
-        cache.k.copy_(k0)
-        cache.v.copy_(v0)
-        if flush is not None:
-            flush.fill_(1)
-
-    def step():
-        tk.tri_compress_step(cache, stats, params, idx_out=idx, new_len=new_len, ws=ws, stream=stream,
-                             compact=args.compact)
-
-    for _ in range(args.warmup):
-        restore()
-        step()
-    torch.cuda.synchronize()
-    assert tk.tri_get_device_status() == 0
-
-    # algorithmic bytes: K read for scoring + K/V moved (read + write) by
-    # compaction, over the units the step compresses (N > B)
-    B, rb = w.budget, w.d * w.esize
-    lens = [int(x) for x in data["seq_len"].tolist()]
-    M = _moved_rows(idx, data["seq_len"], B) if args.compact == "ordered" else _moved_rows_holefill(idx, data["seq_len"], B)
-    units = L * w.S * w.Hkv
-    n_keys = L * w.Hkv * sum(lens)
-    scored = L * w.Hkv * sum(n for n in lens if n > B)
-    units_c = L * w.Hkv * sum(1 for n in lens if n > B)
-    alg_bytes = scored * rb + 4 * M * rb
-    alg_bytes_full_move = scored * rb + 4 * units_c * B * rb
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        torch.cuda.nvtx.range_push("timed")
-        for i in range(args.steps):
-            restore()
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
-    if world > 1:
-        dist.barrier()
-    ms = [a.elapsed_time(b) for a, b in ev]
-    t_step = sum(ms) / len(ms) / 1e3
-    t_step = max_over_ranks(t_step, dev)
-    assert tk.tri_get_device_status() == 0
+    m = Measured(tk, w, dev)
+    t_step, ms, clocks = m.time(args.compact, args.steps, args.warmup, world, local)
+    b = m.bytes(args.compact)
+    head_kernel = _kernel_name(w, m.cache.cap, args.compact, m.launches)
+    head_launches, head_L = m.launches, m.L
+    l2_note = (f"cache restored from a pristine {m.cache_bytes / 1e9:.3f} GB copy before every step"
+               + (" plus a 256 MB L2 flush" if m.flush is not None else " (flushes L2)") + "; untimed")
 
     # end to end through the public API from pinned host buffers
     e2e = None
     if args.e2e_steps > 0:
         e2e_steps = min(args.steps, args.e2e_steps)
-        t_e2e, h2d, d2h = run_e2e(tk, cache, stats, params, k0, v0, idx, new_len, e2e_steps, args.compact)
-        e2e = {"value": world * n_keys / t_e2e, "unit": "keys/s", "h2d_bytes_per_step": h2d,
+        t_e2e, h2d, d2h = run_e2e(tk, m.cache, m.stats, m.params, m.k0, m.v0, m.idx, m.new_len, e2e_steps,
+                                  args.compact)
+        e2e = {"value": world * b["n_keys"] / t_e2e, "unit": "keys/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "how": "layer-pipelined: layer l's K/V up, layer l-1 compressed, layer l-2's K/V, idx down, "
                       "on three streams"}
+
+    extras = {}
+    if args.extras and w.name == WORKLOAD and args.layers is None and args.seqs is None:
+        other = "holefill" if args.compact == "ordered" else "ordered"
+        extras[f"{w.name}/{other}"] = _extra(m, other, args.steps, args.warmup, world, local, peak,
+                                             "same cache and step, the other compaction layout")
+        m.free()
+        m = Measured(tk, WORKLOADS["qwen3_8b_36l_b4_n32768"], dev)
+        extras["qwen3_8b_36l_b4_n32768"] = _extra(m, "ordered", args.extra_steps, args.warmup, world, local, peak,
+                                                  "long one-shot compression, 32768 -> 2048 keys")
+        m.free()
+        pw = WORKLOADS["qwen3_32b_64l_b64_paged"]
+        m = Measured(tk, pw.with_(L=args.paged_layers), dev)
+        extras[f"qwen3_32b_64l_b64_paged/layers0-{args.paged_layers - 1}"] = _extra(
+            m, "ordered", args.extra_steps, args.warmup, world, local, peak,
+            f"layer group of {args.paged_layers} of the 64 layers (K+V of all 64, ~293 GB, exceed HBM); every "
+            "layer has the same lengths and block table, so the group's per-key throughput is the step's")
+        m.free()
+        extras["decode_loop_qwen3_8b_36l_b16_paged"] = decode_leg(tk, dev, args.decode_windows, 1, world, local,
+                                                                 peak)
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
-    peak, peak_kind = _peaks()
-    achieved = alg_bytes / t_step / 1e9
-    mma = w.dtype == "bf16" and w.pairing == "half"
-    if launches == 1:
-        kname = f"fused_mma_kernel<{w.d},{w.G}>" if mma else f"fused_kernel<{w.d},{w.G},{w.dtype}>"
-    else:
-        kname = ("phase_kernel+" + ("score_tiles_mma_kernel" if mma else "score_tiles_kernel")
-                 + "+" + _select_kernel_name(w, cache.cap, args.compact))
+    achieved = b["alg_bytes"] / t_step / 1e9
     line = {
-        "metric": METRIC, "value": job_throughput(world, n_keys, t_step), "unit": "keys/s", "n_gpus": world,
+        "metric": METRIC, "value": job_throughput(world, b["n_keys"], t_step), "unit": "keys/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "accum": "f32",
         "data": "synthetic",
-        "config": _config(w, {"layers": L, "compaction": args.compact,
-                              "l2": f"cache restored from a pristine {cache_bytes / 1e9:.3f} GB copy before every "
-                                    "step" + (" plus a 256 MB L2 flush" if flush is not None else " (flushes L2)")
-                                    + "; untimed",
+        "config": _config(w, {"layers": head_L, "compaction": args.compact,
+                              "l2": l2_note,
                               "parallelism": f"replicas x{world}"}),
         "compress_step_us": t_step * 1e6,
         "hbm_gbs": achieved,
         "hbm_frac_of_8tbs": achieved / 8000.0,
-        "moved_rows": M, "moved_rows_if_all_B": units_c * B, "units": units, "units_compressed": units_c,
+        "moved_rows": b["moved_rows"], "moved_rows_if_all_B": b["moved_rows_if_all_B"], "units": b["units"],
+        "units_compressed": b["units_compressed"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": _traffic_record(kernel_src_hash(), w.name, L),
-                     "algorithmic_bytes_per_launch": alg_bytes,
-                     "algorithmic_bytes_if_all_B_moved": alg_bytes_full_move,
-                     "kernel": kname},
+                     "traffic": _traffic_record(kernel_src_hash(), w.name, w.L),
+                     "algorithmic_bytes_per_launch": b["alg_bytes"],
+                     "algorithmic_bytes_if_all_B_moved": b["alg_bytes_all_B"],
+                     "kernel": head_kernel},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "clocks": clk.summary(),
-        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+        "gpu_launches": head_launches * args.steps,
         "step_ms_min": min(ms), "step_ms_median": float(np.median(ms)),
+        "extras": extras or None,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -443,7 +664,8 @@ def run_b300(args, w):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of this run; for N > 1 launch one rank per GPU with torchrun (WORLD_SIZE must be N)")
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
@@ -460,7 +682,18 @@ def main():
                     help="layout of the kept rows (default: ordered, the slot order of the kept keys)")
     ap.add_argument("--seqs", type=int, default=None,
                     help="use only N sequences (small case for ncu captures)")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="time only the headline workload (skip the hole-fill, long and paged extras)")
+    ap.add_argument("--extra-steps", type=int, default=20, help="timed steps of each extra workload")
+    ap.add_argument("--decode-windows", type=int, default=2,
+                    help="timed 128-token windows of the decode-loop extra")
+    ap.add_argument("--paged-layers", type=int, default=8,
+                    help="layers of the paged Qwen3-32B-shaped workload timed as its extra (a layer group)")
     args = ap.parse_args()
+    if args.gpus != _world():
+        sys.stderr.write(f"bench.py: --gpus {args.gpus} but WORLD_SIZE is {_world()}; for N > 1 launch one rank "
+                         "per GPU with `python -m torch.distributed.run --nproc-per-node N bench.py --gpus N`\n")
+        sys.exit(2)
     from synth import WORKLOADS
     w = WORKLOADS[args.workload]
     if args.layers:
