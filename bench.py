@@ -216,29 +216,32 @@ class ClockSampler:
 def _traffic_record(kernel_src_hash, workload, layers):
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source and this workload
-    (else None)."""
+    (else None).  A capture taken on the first `captured_layers` layers (a
+    case of a few GB, as ncu captures should be) is scaled to `layers`: every
+    layer holds the same units, so the traffic grows in proportion."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f)
-        if (rec.get("kernel_src_sha1") == kernel_src_hash and rec.get("workload") == workload
-                and int(rec.get("layers", layers)) == layers):
-            return float(rec["dram_bytes_per_launch"])
+        if rec.get("kernel_src_sha1") == kernel_src_hash and rec.get("workload") == workload:
+            cl = int(rec.get("captured_layers", rec.get("layers", layers)))
+            return float(rec["dram_bytes_per_launch"]) * layers / cl
     except Exception:
         pass
     return None
 
 
 def _select_kernel_name(w, cap, compact):
-    """The long-unit select/compact kernel tri_compress_step launches: the
-    three-per-SM select2_kernel when its shared memory holds the kept list and,
-    for hole-fill, the hole bookkeeping (B + 16 + 4 min(B, cap - B) bytes in a
-    4 x 16 KB ring); else select_compact_kernel."""
+    """The long-unit select/compact kernels tri_compress_step launches:
+    select_only_kernel then compact_only_kernel when the compaction's shared
+    memory (a 6 x 16 KB ring, 96 barrier bytes, 256 selection bytes, the kept
+    list) fits 227 KB and, for hole-fill, the ring holds the hole bookkeeping
+    (B + 16 + 4 min(B, cap - B) bytes); else select_compact_kernel."""
     B = w.budget
     bcap = -(-min(B, cap) // 32) * 32
-    total = 4 * 16384 + 64 + 1024 + 256 + 128 + -(-bcap * 4 // 128) * 128
-    hf_ok = compact != "holefill" or B + 16 + 4 * max(min(B, cap - B), 0) <= 4 * 16384
-    return "select2_kernel" if total <= 232448 and hf_ok else "select_compact_kernel"
+    total = 6 * 16384 + 2 * 6 * 8 + 256 + -(-bcap * 4 // 128) * 128
+    hf_ok = compact != "holefill" or B + 16 + 4 * max(min(B, cap - B), 0) <= 6 * 16384
+    return "select_only_kernel+compact_only_kernel" if total <= 232448 and hf_ok else "select_compact_kernel"
 
 
 def kernel_src_hash():
@@ -355,7 +358,7 @@ def _kernel_name(w, cap, compact, launches):
     mma = w.dtype == "bf16" and w.pairing == "half"
     if launches == 1:
         return f"fused_mma_kernel<{w.d},{w.G}>" if mma else f"fused_kernel<{w.d},{w.G},{w.dtype}>"
-    return ("phase_kernel+" + ("score_tiles_mma_kernel" if mma else "score_tiles_kernel") + "+"
+    return ("phase_kernel+" + ("score_keys_mma_kernel" if mma else "score_tiles_kernel") + "+"
             + _select_kernel_name(w, cap, compact))
 
 
@@ -374,7 +377,9 @@ class Measured:
         d["q_pre"] = None
         self.params = tk.Params(w.theta, d["t"], w.offsets, w.budget, pairing=w.pairing)
         self.ws = tk.workspace(self.cache, self.stats, self.params)
-        self.launches = 1 if self.ws is None else 3   # fused kernel, or phases + score tiles + select/compact
+        # fused kernel, or phases + scores + (select, compact | select/compact)
+        self.launches = (1 if self.ws is None else
+                         2 + len(_select_kernel_name(w, self.cache.cap, "ordered").split("+")))
         self.k0, self.v0 = self.cache.k.clone(), self.cache.v.clone()
         self.L = self.cache.L
         self.idx = torch.empty((self.L, w.S, w.Hkv, w.budget), dtype=torch.int32, device=dev)
@@ -687,6 +692,8 @@ def main():
     ap.add_argument("--extra-steps", type=int, default=20, help="timed steps of each extra workload")
     ap.add_argument("--decode-windows", type=int, default=2,
                     help="timed 128-token windows of the decode-loop extra")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run only the decode-loop workload and print its record (for profiling)")
     ap.add_argument("--paged-layers", type=int, default=8,
                     help="layers of the paged Qwen3-32B-shaped workload timed as its extra (a layer group)")
     args = ap.parse_args()
@@ -702,6 +709,13 @@ def main():
         w = w.with_(S=args.seqs)
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.decode_only:
+        import torch
+        import kv_cache_compression_06_b300 as tk
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        res = decode_leg(tk, torch.device("cuda", local), args.decode_windows, 1, 1, local, _peaks()[0])
+        print(json.dumps(res), flush=True)
     else:
         run_b300(args, w)
 

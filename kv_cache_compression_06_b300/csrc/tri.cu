@@ -12,10 +12,18 @@
 //                        bulk-copy compaction.  Also the score-only variant
 //                        behind tri_score.
 //   score_tiles_kernel   a1+a2 for long units, 2048 keys per CTA (same pipeline):
-//                        raw scores and per-tile (mean, M2) to the workspace.
+//                        raw scores and per-tile (mean, M2) to the workspace
+//                        (tri_score; the compress step with fp32 or interleaved
+//                        caches).  score_tiles_mma_kernel: its tensor-core form.
+//   score_keys_mma_kernel a1+a2 of the compress step for long bf16 units:
+//                        key-major raw scores straight from the MMA fragments,
+//                        moments in registers, one (mean, M2) per CTA.
+//   select_only_kernel   a3+a4 of the compress step for long units: kept slots.
+//   compact_only_kernel  a5 of the compress step for long units.
 //   zmax_kernel          a3 for long units (tri_score): Chan-merged moments -> agg.
-//   select_compact_kernel a3..a5 for long units (from raw scores), tri_select_topb
-//                        (from agg) and tri_compact_kv (from idx).
+//   select_compact_kernel a3..a5 for long units whose kept list or hole-fill
+//                        bookkeeping does not fit compact_only_kernel,
+//                        tri_select_topb (from agg) and tri_compact_kv (from idx).
 //   calib_*_kernel       streamed calibration: sums per (layer, head, band) that
 //                        chunks of samples add to, merged, then finalised.
 //   *_curve_kernel       distance-preference curves (centers vs exact logits).
@@ -122,7 +130,7 @@ struct FusedLayout {
   __host__ __device__ FusedLayout(int G, int F, int capp) {
     sstride = capp + 4;
     int o = kRingBytes;
-    bars = o;   o += 128;                 // kStages score barriers + kStages compaction barriers
+    bars = o;   o += 256;                 // score barriers, 2 x kStages compaction barriers, flags
     wts = o;    o += align_up(G * 3 * F * 4, 128);
     red = o;    o += 512;
     hist = o;   o += 1024;
@@ -228,14 +236,15 @@ __global__ void __launch_bounds__(kFusedThreads, (G <= 4 ? 2 : 1)) fused_kernel(
   if ((tid >> 5) == 0) compact_unit_runs(c, l, s, g, idxs, e0, B, N, ring, bars + kStages);
 }
 
-// Pipe over the barrier block of a layout: full[4] | empty[4] | compaction[4] | fail, issued.
+// Pipe over the barrier block of a layout (256 bytes): full[4] | empty[4] |
+// compaction[2][4] | fail, issued.
 __device__ __forceinline__ Pipe make_pipe(char *smem, int bars) {
   uint64_t *b = reinterpret_cast<uint64_t *>(smem + bars);
   Pipe p;
   p.ring = smem;
   p.full = b;
   p.empty = b + kStages;
-  p.fail = reinterpret_cast<volatile int *>(b + 3 * kStages);
+  p.fail = reinterpret_cast<volatile int *>(b + 4 * kStages);
   p.issued = p.fail + 1;
   return p;
 }
@@ -272,7 +281,7 @@ struct TileLayout {
   int bars, wts, red, scores, total;
   __host__ __device__ TileLayout(int G, int F) {
     int o = kRingBytes;
-    bars = o;   o += 128;
+    bars = o;   o += 256;
     wts = o;    o += align_up(G * 3 * F * 4, 128);
     red = o;    o += 512;
     scores = o; o += G * tile_stride_for(G) * 4;
@@ -549,10 +558,13 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
 // runs the same z/max, select and compaction as fused_kernel.
 struct FusedMmaArgs {
   CUtensorMap ks;   // 128B-swizzled K map (as TileArgs::ks)
+  TmaMaps maps;     // paged caches: block maps for the compaction's tensor stores
   FusedArgs f;
 };
 
-template <int D, int G>
+// PB: paged cache with block maps (two-warp compaction with row gathers and
+// block stores); otherwise warp 0's run copies.
+template <int D, int G, bool PB>
 __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
     fused_mma_kernel(const __grid_constant__ FusedMmaArgs A) {
   const FusedArgs &a = A.f;
@@ -598,11 +610,15 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   }
   if (len_writer) a.new_len[s] = B;
   const int ss = lay.sstride;
+  // paged caches compact with two warps (K and V), row gathers and block
+  // stores; dense ones with warp 0's run copies
+  constexpr bool blk_compact = PB;
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&pipe.full[st], 1);
       mbar_init(&pipe.empty[st], SPS);
-      mbar_init(&cbars[st], 1);
+      mbar_init(&cbars[st], blk_compact ? kCompactArrivals : 1);
+      mbar_init(&cbars[kStages + st], kCompactArrivals);
     }
     *pipe.fail = 0;
     *pipe.issued = 0;
@@ -684,7 +700,11 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   // The ring was last read by ldmatrix (generic proxy); TMA writes it next.
   fence_proxy_async_smem();
   __syncthreads();
-  if (warp == 0) compact_unit_runs(c, l, s, g, idxs, e0, B, N, ring, cbars);
+  if constexpr (PB) {
+    if (warp < 2) compact_unit_tma(c, &A.maps, warp, l, s, g, idxs, e0, B, N, ring, kStages, cbars + warp * kStages);
+  } else {
+    if (warp == 0) compact_unit_runs(c, l, s, g, idxs, e0, B, N, ring, cbars);
+  }
 }
 
 // Chan's combination of (count, mean, M2) summaries: (n, mean, M2) absorbs (nb, mb, Mb).
@@ -707,11 +727,11 @@ __device__ __forceinline__ void chan_merge(float &n, float &mean, float &M2, flo
 // writes mean and 1/std (0 if std = 0) to mom[h], mom[8 + h].  Needs blockDim
 // >= 32 * G; the caller synchronises before reading mom.
 __device__ __forceinline__ void merge_tile_moments(const float2 *part, long long u, int ntiles, int G,
-                                                   int N, float *mom) {
+                                                   int N, float *mom, int part_keys) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp >= G) return;
   const int h = warp;
-  const int TK = tile_keys_for(G);
+  const int TK = part_keys;
   const int used = (N + TK - 1) / TK;
   float n = 0.f, mean = 0.f, M2 = 0.f;
   for (int t = lane; t < used; t += 32) {
@@ -740,6 +760,184 @@ __device__ __forceinline__ void merge_tile_moments(const float2 *part, long long
   }
 }
 
+// ---------------------------------------------------------------- long units: key-major scores
+// The compress step's long-unit score kernel (bf16 caches, rotate-half bands).
+// As score_tiles_mma_kernel, but each 16-key tile's scores go straight from the
+// MMA fragments to the workspace in key-major order (key i's G scores at
+// raw[(u*capp + i)*G + h]: a quad of lanes holds one key's heads, so the warp
+// writes whole 256-byte (G = 8) or 128-byte (G = 4) runs), and every lane keeps
+// shifted sums of its heads' scores in registers.  There is no per-tile
+// epilogue: the consumers never stop streaming.  At the end the lanes' (count,
+// mean, M2) merge (Chan) into one entry per CTA and head in `part`.
+constexpr int kKmCtaKeys = 8192;   // keys per CTA (one part entry)
+constexpr int kKmStages = 6;       // ring stages (the score tile buffer is gone)
+
+struct KmLayout {
+  int bars, wts, red, total;
+  __host__ __device__ KmLayout(int G, int F) {
+    int o = kKmStages * kStageBytes;
+    bars = o;  o += 256;                       // full[6], empty[6], fail, issued
+    wts = o;   o += align_up(G * 3 * F * 4, 128);
+    red = o;   o += kConsumerWarps * 4 * 5 * 4;   // per warp and lane class: n, mean[2], M2[2]
+    total = o;
+  }
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 2) score_keys_mma_kernel(const __grid_constant__ TileArgs a) {
+  constexpr int F = D / 2;
+  constexpr int TR = kStageBytes / (2 * D);
+  constexpr int SPS = TR / 16;
+  constexpr int GROUPS = kConsumerWarps / SPS;
+  constexpr int NC = kConsumerWarps * 32;
+  extern __shared__ __align__(1024) char smem[];
+  const KmLayout lay(G, F);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  uint64_t *empty = full + kKmStages;
+  volatile int *fail = reinterpret_cast<volatile int *>(empty + kKmStages);
+  volatile int *issued = fail + 1;
+  float *wts = reinterpret_cast<float *>(smem + lay.wts);
+  float *red = reinterpret_cast<float *>(smem + lay.red);
+  const CacheView &c = a.c;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u = blockIdx.y;
+  const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
+  if (timed_out()) return;
+  const int N = c.seq_len[s];
+  if (N < 0 || N > c.cap) {
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  if (a.skip_small && N <= a.budget) return;
+  const int i0 = blockIdx.x * kKmCtaKeys;
+  if (i0 >= N) return;
+  const int n = min(kKmCtaKeys, N - i0);
+  if (!c.blocks_ok(s, n, i0)) {
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  if (tid == 0) {
+    for (int st = 0; st < kKmStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], SPS);
+    }
+    *fail = 0;
+    *issued = 0;
+    fence_mbar_init();
+  }
+  build_weights<G, F>(wts, a.center, a.R, a.mag, a.Hq, l, g, a.t[s], a.sc, a.phase + (long long)s * F);
+  __syncthreads();
+  const int nst = (n + TR - 1) / TR;
+  const long long urow0 = (long long)u * c.cap;
+  // lane state: shifted sums of the two heads n0, n0 + 1 of this lane
+  const int r = lane >> 2, n0 = 2 * (lane & 3);
+  const bool holds = G == 8 || n0 < G;
+  float cnt = 0.f, sh[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f}, s2[2] = {0.f, 0.f};
+  if (warp == kProducerWarp) {
+    int t = 0;
+    for (; t < nst; ++t) {
+      const int st = t % kKmStages;
+      if (*fail || (t >= kKmStages && !mbar_wait(&empty[st], (uint32_t)(((t / kKmStages) - 1) & 1)))) {
+        *fail = 1;
+        break;
+      }
+      produce_stage_sw<D>(c, &a.ks, l, s, g, urow0, i0 + t * TR, min(TR, n - t * TR), smem + st * kStageBytes,
+                          &full[st], lane);
+    }
+    if (lane == 0) *issued = t;
+  } else {
+    MmaWeights<D, G> w;
+    load_mma_weights<D, G>(w, wts, NC, warp == 0);
+    const int grp = warp / SPS, sub = warp % SPS;
+    const uint32_t ring = smem_u32(smem);
+    float *raw_c = a.raw + ((long long)u * a.raw_stride + i0) * G;   // this CTA's first key
+    const int blk = c.paged() ? c.block : 0;
+    for (int t = grp; t < nst; t += GROUPS) {
+      const int st = t % kKmStages;
+      if (!*fail && !mbar_wait(&full[st], (uint32_t)((t / kKmStages) & 1))) *fail = 1;
+      float o[4];
+      score_tile_mma_frag<D, G, TR>(ring + st * kStageBytes, 16 * sub, w, blk, o);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);   // the stage's rows are in registers
+      if (*fail) continue;
+      const int kb = t * TR + 16 * sub;         // CTA-local key of this tile's row 0
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int key = kb + r + 8 * hh;
+        if (holds && key < n) {
+          const float x0 = o[2 * hh], x1 = o[2 * hh + 1];
+          if constexpr (G == 1)
+            raw_c[key] = x0;
+          else
+            *reinterpret_cast<float2 *>(raw_c + (long long)key * G + n0) = make_float2(x0, x1);
+          if (cnt == 0.f) {
+            sh[0] = x0;
+            sh[1] = x1;
+          }
+          const float d0 = x0 - sh[0], d1 = x1 - sh[1];
+          s1[0] += d0;
+          s1[1] += d1;
+          s2[0] = fmaf(d0, d0, s2[0]);
+          s2[1] = fmaf(d1, d1, s2[1]);
+          cnt += 1.f;
+        }
+      }
+    }
+    // this lane's (count, mean, M2) per head slot, merged over the lanes of
+    // the same class (lane % 4: same heads), then written per warp
+    float mean[2], m2[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      mean[j] = cnt > 0.f ? sh[j] + s1[j] / cnt : 0.f;
+      m2[j] = cnt > 0.f ? fmaxf(s2[j] - s1[j] * s1[j] / cnt, 0.f) : 0.f;
+    }
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+      const float nb = __shfl_xor_sync(0xffffffffu, cnt, off);
+      float mb[2], qb[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        mb[j] = __shfl_xor_sync(0xffffffffu, mean[j], off);
+        qb[j] = __shfl_xor_sync(0xffffffffu, m2[j], off);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float nn = cnt;
+        chan_merge(nn, mean[j], m2[j], nb, mb[j], qb[j]);
+      }
+      cnt += nb;
+    }
+    if (lane < 4) {
+      float *rw = red + (warp * 4 + lane) * 5;
+      rw[0] = cnt;
+      rw[1] = mean[0];
+      rw[2] = mean[1];
+      rw[3] = m2[0];
+      rw[4] = m2[1];
+    }
+  }
+  __syncthreads();
+  if (*fail) {
+    if (tid == 0) {
+      const int iss = *issued;
+      for (int st = 0; st < kKmStages && st < iss; ++st) {
+        const int last = st + ((iss - 1 - st) / kKmStages) * kKmStages;
+        mbar_wait(&full[st], (uint32_t)((last / kKmStages) & 1));
+      }
+    }
+    return;
+  }
+  if (tid < G) {
+    const int cls = tid / 2, j = tid & 1;
+    float nn = 0.f, mm = 0.f, qq = 0.f;
+    for (int wp = 0; wp < kConsumerWarps; ++wp) {
+      const float *rw = red + (wp * 4 + cls) * 5;
+      chan_merge(nn, mm, qq, rw[0], rw[1 + j], rw[3 + j]);
+    }
+    a.part[((long long)u * a.ntiles + blockIdx.x) * G + tid] = make_float2(mm, qq);
+  }
+}
+
 struct ZArgs {
   int S, Hkv, G, ntiles;
   long long cap, raw_stride;
@@ -757,7 +955,7 @@ __global__ void __launch_bounds__(256) zmax_kernel(const ZArgs a) {
   if (N < 0 || N > a.cap) return;
   const int i0 = tile * tile_keys_for(a.G);
   if (i0 >= N) return;
-  merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom);
+  merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom, tile_keys_for(a.G));
   __syncthreads();
   const int i1 = min(N, i0 + tile_keys_for(a.G));
   for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
@@ -781,7 +979,11 @@ struct SCArgs {
   const float *agg;
   const int *idx_in;
   int *idx_out, *new_len;
-  uint32_t *keys;   // select2_kernel: workspace [units][capp] (16-byte aligned rows)
+  uint32_t *keys;   // select_only_kernel: workspace [units][capp] (16-byte aligned rows)
+  int raw_km;       // mode 0: raw is key-major [(u*capp + i)*G + h] (else head-major)
+  int part_keys;    // mode 0: keys covered by one (mean, M2) entry of part
+  int *kept;        // select_only / compact_only: kept slots [units][budget] (idx_out or workspace)
+  int *e0s;         // select_only / compact_only: first dropped slot per unit (workspace)
 };
 
 // The keys (one u32 per slot) and the compaction ring share one region at the
@@ -870,6 +1072,65 @@ __device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *
   }
 }
 
+// a3 from key-major raw scores: key i's G scores are raw_u[i*G .. i*G + G)
+// (16-byte aligned rows of 4 keys); each thread takes quads of keys (G 16-byte
+// loads, contiguous across threads) and writes their order-preserving keys.
+// Key slots in [N, round4(N)) receive don't-care values.
+template <int G>
+__device__ void zmax_from_raw_km(const float *raw_u, int N, const float *mom, uint32_t *keys) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  float mu[G], iv[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    mu[h] = mom[h];
+    iv[h] = mom[8 + h];
+  }
+  const int n4 = (N + 3) / 4;
+  const float4 *rows = reinterpret_cast<const float4 *>(raw_u);
+  for (int q = tid; q < n4; q += nt) {
+    float x[4 * G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const float4 v = __ldg(rows + (long long)q * G + k);
+      x[4 * k] = v.x;
+      x[4 * k + 1] = v.y;
+      x[4 * k + 2] = v.z;
+      x[4 * k + 3] = v.w;
+    }
+    uint32_t kk[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float z = (x[j * G] - mu[0]) * iv[0];
+#pragma unroll
+      for (int h = 1; h < G; ++h) z = fmaxf(z, (x[j * G + h] - mu[h]) * iv[h]);
+      kk[j] = score_key(z);
+    }
+    reinterpret_cast<uint4 *>(keys)[q] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+  }
+}
+
+// zmax_from_raw or zmax_from_raw_km for the unit's G.
+template <bool PF>
+__device__ __forceinline__ void zmax_dispatch(const SCArgs &a, long long u, int N, const float *mom,
+                                              uint32_t *keys) {
+  const float *raw_u = a.raw + u * a.G * a.capp;
+  if (a.raw_km) {
+    switch (a.G) {
+      case 1: zmax_from_raw_km<1>(raw_u, N, mom, keys); break;
+      case 2: zmax_from_raw_km<2>(raw_u, N, mom, keys); break;
+      case 4: zmax_from_raw_km<4>(raw_u, N, mom, keys); break;
+      default: zmax_from_raw_km<8>(raw_u, N, mom, keys); break;
+    }
+    return;
+  }
+  switch (a.G) {
+    case 1: zmax_from_raw<1, PF>(raw_u, a.capp, N, mom, keys); break;
+    case 2: zmax_from_raw<2, PF>(raw_u, a.capp, N, mom, keys); break;
+    case 4: zmax_from_raw<4, PF>(raw_u, a.capp, N, mom, keys); break;
+    default: zmax_from_raw<8, PF>(raw_u, a.capp, N, mom, keys); break;
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __grid_constant__ SCArgs a) {
   extern __shared__ __align__(1024) char smem[];
   const SCLayout lay(a.capp, a.bcap);
@@ -906,8 +1167,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
   if (len_writer) a.new_len[s] = B;
   if (tid == 0) {
     for (int st = 0; st < lay.nstages; ++st) {
-      mbar_init(&cbars[st], 1);                       // K warp
-      mbar_init(&cbars[kMaxCompactStages + st], 1);   // V warp
+      mbar_init(&cbars[st], kCompactArrivals);                       // K warp
+      mbar_init(&cbars[kMaxCompactStages + st], kCompactArrivals);   // V warp
     }
     fence_mbar_init();
   }
@@ -939,15 +1200,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
     return;
   }
   if (a.mode == 0) {
-    merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom);
+    merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom, a.part_keys);
     __syncthreads();
-    const float *raw_u = a.raw + (long long)u * a.G * a.capp;
-    switch (a.G) {
-      case 1: zmax_from_raw<1>(raw_u, a.capp, N, mom, keys); break;
-      case 2: zmax_from_raw<2>(raw_u, a.capp, N, mom, keys); break;
-      case 4: zmax_from_raw<4>(raw_u, a.capp, N, mom, keys); break;
-      default: zmax_from_raw<8>(raw_u, a.capp, N, mom, keys); break;
-    }
+    zmax_dispatch<true>(a, u, N, mom, keys);
   } else {
     for (int i = tid; i < N; i += nt) keys[i] = score_key(a.agg[(long long)u * c.cap + i]);
   }
@@ -973,39 +1228,23 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
   }
 }
 
-// ---------------------------------------------------------------- long units: select/compact, three per SM
-// The compress step's long-unit select/compact (select_compact_kernel mode 0)
-// with its keys in the workspace instead of shared memory: 256 threads, at
-// most 80 registers, a 4-stage compaction ring, ~70-75 KB of shared memory, so
-// three CTAs (units) share an SM and the latency-bound phases of one unit (z/max
-// loads, radix and kept-list passes over its keys in L2) overlap the others'
-// compaction traffic.  The z/max loads are single-buffered here (the extra
-// CTAs supply the memory-level parallelism).
-constexpr int kSel2Threads = 256;
-constexpr int kSel2Stages = 4;
+// ---------------------------------------------------------------- long units: select, then compact
+// The compress step's long-unit selection and compaction as two kernels.  The
+// selection's passes over a unit's keys (z/max from the raw scores, four radix
+// passes, two kept-list passes; keys in the workspace, L2-resident) are bound
+// by L2 latency, not bandwidth, so select_only_kernel keeps almost nothing in
+// shared memory and many units share an SM; it writes each unit's kept slots
+// and first dropped slot.  compact_only_kernel then only moves rows: two CTAs
+// per SM, each with a K warp and a V warp on 6-stage rings, so the bytes in
+// flight per SM stay high for the whole kernel.
+constexpr int kSelOnlyThreads = 256;
+constexpr int kCoThreads = 256;
+constexpr int kCoStages = 6;
 
-struct Sel2Layout {
-  int bars, hist, sm, mom, idx, total;
-  __host__ __device__ explicit Sel2Layout(int bcap) {
-    int o = kSel2Stages * kStageBytes;   // ring (also the hole-fill bookkeeping)
-    bars = o; o += 2 * kSel2Stages * 8;
-    hist = o; o += 1024;
-    sm = o;   o += kSelInts * 4;
-    mom = o;  o += 128;
-    idx = o;  o += align_up(bcap * 4, 128);
-    total = o;
-  }
-};
-
-__global__ void __launch_bounds__(kSel2Threads, 3) select2_kernel(const __grid_constant__ SCArgs a) {
-  extern __shared__ __align__(1024) char smem[];
-  const Sel2Layout lay(a.bcap);
-  char *ring = smem;
-  uint64_t *cbars = reinterpret_cast<uint64_t *>(smem + lay.bars);
-  uint32_t *hist = reinterpret_cast<uint32_t *>(smem + lay.hist);
-  int *sm = reinterpret_cast<int *>(smem + lay.sm);
-  float *mom = reinterpret_cast<float *>(smem + lay.mom);
-  int *idxs = reinterpret_cast<int *>(smem + lay.idx);
+__global__ void __launch_bounds__(kSelOnlyThreads) select_only_kernel(const __grid_constant__ SCArgs a) {
+  __shared__ uint32_t hist[256];
+  __shared__ int sm[kSelInts];
+  __shared__ float mom[32];
   const CacheView &c = a.c;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int u = blockIdx.x;
@@ -1030,37 +1269,63 @@ __global__ void __launch_bounds__(kSel2Threads, 3) select2_kernel(const __grid_c
     return;
   }
   if (len_writer) a.new_len[s] = B;
-  if (tid == 0) {
-    for (int st = 0; st < kSel2Stages; ++st) {
-      mbar_init(&cbars[st], 1);                  // K warp
-      mbar_init(&cbars[kSel2Stages + st], 1);    // V warp
-    }
-    fence_mbar_init();
-  }
-  merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom);
+  merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom, a.part_keys);
   __syncthreads();
   uint32_t *keys = a.keys + (long long)u * a.capp;
-  const float *raw_u = a.raw + (long long)u * a.G * a.capp;
-  switch (a.G) {
-    case 1: zmax_from_raw<1, false>(raw_u, a.capp, N, mom, keys); break;
-    case 2: zmax_from_raw<2, false>(raw_u, a.capp, N, mom, keys); break;
-    case 4: zmax_from_raw<4, false>(raw_u, a.capp, N, mom, keys); break;
-    default: zmax_from_raw<8, false>(raw_u, a.capp, N, mom, keys); break;
-  }
+  zmax_dispatch<false>(a, u, N, mom, keys);
   __syncthreads();   // the keys (global) are visible to the whole CTA
   int ntie;
   const uint32_t T = radix_select_gmem(keys, N, B, hist, sm, &ntie);
-  const int e0 = build_kept_gmem(keys, N, B, T, ntie, idxs, sm);
+  const int e0 = build_kept_gmem(keys, N, B, T, ntie, a.kept + (long long)u * B, sm);
+  if (tid == 0) a.e0s[u] = e0;
+}
+
+struct CoLayout {
+  int bars, sm, idx, total;
+  __host__ __device__ explicit CoLayout(int bcap) {
+    int o = kCoStages * kStageBytes;   // ring (also the hole-fill bookkeeping)
+    bars = o; o += 2 * kCoStages * 8;
+    sm = o;   o += kSelInts * 4;
+    idx = o;  o += align_up(bcap * 4, 128);
+    total = o;
+  }
+};
+
+__global__ void __launch_bounds__(kCoThreads, 2) compact_only_kernel(const __grid_constant__ SCArgs a) {
+  extern __shared__ __align__(1024) char smem[];
+  const CoLayout lay(a.bcap);
+  char *ring = smem;
+  uint64_t *cbars = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  int *sm = reinterpret_cast<int *>(smem + lay.sm);
+  int *idxs = reinterpret_cast<int *>(smem + lay.idx);
+  const CacheView &c = a.c;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int u = blockIdx.x;
+  const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
+  if (timed_out()) return;
+  const int N = c.seq_len[s];
+  const int B = a.budget;
+  // units the selection left alone (N <= B, N > cap, bad block ids) are left alone here too
+  if (N <= B || N > c.cap) return;
+  if (!c.blocks_ok(s, N)) return;
+  if (tid == 0) {
+    for (int st = 0; st < kCoStages; ++st) {
+      mbar_init(&cbars[st], kCompactArrivals);               // K warp
+      mbar_init(&cbars[kCoStages + st], kCompactArrivals);   // V warp
+    }
+    fence_mbar_init();
+  }
+  const int *kept = a.kept + (long long)u * B;
+  for (int j = tid; j < B; j += nt) idxs[j] = kept[j];
+  const int e0 = a.e0s[u];
+  __syncthreads();
   if (a.holefill) {
     holefill_unit(c, l, s, g, idxs, B, N, ring, sm, a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
     return;
   }
-  if (a.idx_out != nullptr)
-    for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
-  __syncthreads();
   if ((tid >> 5) < 2)
-    compact_unit_tma(c, &a.maps, tid >> 5, l, s, g, idxs, e0, B, N, ring, kSel2Stages,
-                     cbars + (tid >> 5) * kSel2Stages);
+    compact_unit_tma(c, &a.maps, tid >> 5, l, s, g, idxs, e0, B, N, ring, kCoStages,
+                     cbars + (tid >> 5) * kCoStages);
 }
 
 // ================================================================ host side
@@ -1275,9 +1540,9 @@ static bool fused_fits(const tri_cache *c, int G) {
 }
 
 struct SplitWs {
-  size_t raw_off, part_off, phase_off, keys_off, total;
+  size_t raw_off, part_off, phase_off, keys_off, kept_off, e0_off, total;
 };
-static SplitWs split_ws(const tri_cache *c, int G) {
+static SplitWs split_ws(const tri_cache *c, int G, int budget) {
   SplitWs w;
   // raw rows padded to round32(cap) floats: 16-byte aligned for bulk copies
   const size_t raw = (size_t)units_of(c) * G * (size_t)round32(c->cap) * sizeof(float);
@@ -1288,7 +1553,12 @@ static SplitWs split_ws(const tri_cache *c, int G) {
   const size_t keys = (size_t)units_of(c) * (size_t)round32(c->cap) * sizeof(uint32_t);
   w.phase_off = w.part_off + (part + 255) / 256 * 256;
   w.keys_off = w.phase_off + (phase + 255) / 256 * 256;
-  w.total = w.keys_off + (keys + 255) / 256 * 256;
+  // kept slots and first dropped slot per unit (select_only -> compact_only)
+  const size_t kept = (size_t)units_of(c) * (size_t)std::max(budget, 1) * sizeof(int);
+  const size_t e0 = (size_t)units_of(c) * sizeof(int);
+  w.kept_off = w.keys_off + (keys + 255) / 256 * 256;
+  w.e0_off = w.kept_off + (kept + 255) / 256 * 256;
+  w.total = w.e0_off + (e0 + 255) / 256 * 256;
   return w;
 }
 
@@ -1317,8 +1587,9 @@ static tri_status run_fused(const FusedArgs &a, int64_t units, cudaStream_t st) 
       FusedMmaArgs m;
       std::memset(&m, 0, sizeof(m));
       m.f = a;
+      if (a.cache->block_table != nullptr && a.mode == 0) make_maps(a.cache, &m.f.c, &m.maps);
       if (make_swizzled_map(a.cache, a.params, &m.ks)) {
-        auto k = fused_mma_kernel<D, G>;
+        auto k = m.f.c.bt != nullptr && m.f.c.tm_ok ? fused_mma_kernel<D, G, true> : fused_mma_kernel<D, G, false>;
         if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
         k<<<(unsigned)units, kThreads, lay.total, st>>>(m);
         return launch_result();
@@ -1347,6 +1618,25 @@ static tri_status run_tiles(const TileArgs &a, int64_t units, cudaStream_t st) {
   if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
   k<<<dim3((unsigned)a.ntiles, (unsigned)units), kThreads, lay.total, st>>>(a);
   return launch_result();
+}
+
+// The compress step's long-unit scores: the key-major tensor-core kernel for
+// bf16 rotate-half caches (one part entry per CTA of kKmCtaKeys keys), else
+// the CUDA-core tile kernel (head-major, one entry per tile).
+template <int D, int G, bool BF16>
+static tri_status run_keys(const TileArgs &a, int64_t units, cudaStream_t st) {
+  if constexpr (BF16) {
+    if (a.mma_ok) {
+      const KmLayout lay(G, D / 2);
+      auto k = score_keys_mma_kernel<D, G>;
+      if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
+      k<<<dim3((unsigned)a.ntiles, (unsigned)units), kThreads, lay.total, st>>>(a);
+      return launch_result();
+    }
+  }
+  TileArgs b = a;
+  b.mma_ok = 0;
+  return run_tiles<D, G, BF16>(b, units, st);
 }
 
 // Expands a call over the supported (head dim, group size, dtype) instantiations.
@@ -1585,7 +1875,7 @@ tri_status tri_workspace_bytes(const tri_cache *cache, const tri_stats *stats,
   if ((e = check_stats(cache, stats)) != TRI_OK) return e;
   if ((e = check_params(params)) != TRI_OK) return e;
   const int G = stats->Hq / cache->Hkv;
-  *bytes = fused_fits(cache, G) ? 0 : split_ws(cache, G).total;
+  *bytes = fused_fits(cache, G) ? 0 : split_ws(cache, G, params->budget).total;
   return TRI_OK;
 }
 
@@ -1606,7 +1896,7 @@ tri_status tri_score(const tri_cache *cache, const tri_stats *stats, const tri_p
     a.raw = raw;
     return TRI_DISPATCH(run_fused, cache->d, G, bf16, a, units, stream);
   }
-  const SplitWs w = split_ws(cache, G);
+  const SplitWs w = split_ws(cache, G, params->budget);
   if (ws == nullptr || ws_bytes < w.total || !aligned16(ws)) return TRI_ERR_WORKSPACE;
   TileArgs ta = tile_args(cache, stats, params);
   ta.skip_small = 0;
@@ -1691,7 +1981,7 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
     a.new_len = new_len;
     return TRI_DISPATCH(run_fused, cache->d, G, bf16, a, units, stream);
   }
-  const SplitWs w = split_ws(cache, G);
+  const SplitWs w = split_ws(cache, G, params->budget);
   if (ws == nullptr || ws_bytes < w.total || !aligned16(ws)) return TRI_ERR_WORKSPACE;
   SCArgs sa;
   std::memset(&sa, 0, sizeof(sa));
@@ -1711,21 +2001,36 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   ta.raw_stride = sa.capp;
   ta.part = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.part_off);
   ta.phase = reinterpret_cast<const float2 *>(static_cast<char *>(ws) + w.phase_off);
+  if (ta.mma_ok) {   // key-major raw scores, one moment entry per CTA
+    ta.ntiles = (int)((cache->cap + kKmCtaKeys - 1) / kKmCtaKeys);
+    sa.raw_km = 1;
+    sa.part_keys = kKmCtaKeys;
+  } else {
+    sa.raw_km = 0;
+    sa.part_keys = tile_keys_for(G);
+  }
+  sa.ntiles = ta.ntiles;
   if ((e = run_phases(cache, ta, stream)) != TRI_OK) return e;
-  if ((e = TRI_DISPATCH(run_tiles, cache->d, G, bf16, ta, units, stream)) != TRI_OK) return e;
+  if ((e = TRI_DISPATCH(run_keys, cache->d, G, bf16, ta, units, stream)) != TRI_OK) return e;
   sa.raw = ta.raw;
   sa.part = ta.part;
   sa.idx_out = idx_out;
   sa.new_len = new_len;
   sa.keys = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + w.keys_off);
-  // three units per SM when the hole-fill bookkeeping (B bytes + 4 min(B, N - B))
-  // fits the smaller ring; else the one-per-SM kernel with keys in shared memory
-  const Sel2Layout l2(sa.bcap);
+  // selection, then compaction (two kernels), when the compaction's ring holds
+  // the hole-fill bookkeeping (B bytes + 4 min(B, N - B)) and its shared memory
+  // the kept list; else the one-per-SM kernel with keys in shared memory
+  const CoLayout co(sa.bcap);
   const int64_t movers = std::min<int64_t>(params->budget, cache->cap - params->budget);
-  const bool hf_fits = !sa.holefill || params->budget + 16 + 4 * std::max<int64_t>(movers, 0) <= kSel2Stages * kStageBytes;
-  if (l2.total <= kMaxSmem && hf_fits) {
-    if (set_smem(select2_kernel, l2.total) != TRI_OK) return TRI_ERR_CUDA;
-    select2_kernel<<<(unsigned)units, kSel2Threads, l2.total, stream>>>(sa);
+  const bool hf_fits = !sa.holefill || params->budget + 16 + 4 * std::max<int64_t>(movers, 0) <= kCoStages * kStageBytes;
+  if (co.total <= kMaxSmem && hf_fits) {
+    char *wsb = static_cast<char *>(ws);
+    sa.kept = (!sa.holefill && idx_out != nullptr) ? idx_out : reinterpret_cast<int *>(wsb + w.kept_off);
+    sa.e0s = reinterpret_cast<int *>(wsb + w.e0_off);
+    select_only_kernel<<<(unsigned)units, kSelOnlyThreads, 0, stream>>>(sa);
+    if ((e = launch_result()) != TRI_OK) return e;
+    if (set_smem(compact_only_kernel, co.total) != TRI_OK) return TRI_ERR_CUDA;
+    compact_only_kernel<<<(unsigned)units, kCoThreads, co.total, stream>>>(sa);
     return launch_result();
   }
   return run_select_compact(sa, units, stream);

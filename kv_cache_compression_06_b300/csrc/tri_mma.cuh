@@ -227,11 +227,14 @@ __device__ __forceinline__ void produce_stage_sw(const CacheView &c, const CUten
   issue_stage_sw<D>(c, map, l, s, g, urow0, row0, nrows, dst, full, lane);
 }
 
-// Scores the 16 keys at stage rows [r0, r0 + 16) (row0 + r0 + i is the key's
-// index in the caller's score rows); rows at or past nrows are not stored.
+// Scores the 16 keys at stage rows [r0, r0 + 16) into this lane's fragment
+// values: o[e] is the score of key r0 + lane/4 + 8 (e >> 1) for head
+// n + (e & 1), n = 2 (lane % 4).  G = 8: every lane's n is a head; G <= 4: the
+// lo columns are folded into the hi ones, and lanes with n >= G hold nothing
+// meaningful.
 template <int D, int G, int TR>
-__device__ __forceinline__ void score_tile_mma(uint32_t stage, int r0, int nrows, int row0, float *scores,
-                                               int sstride, const MmaWeights<D, G> &w, int blk) {
+__device__ __forceinline__ void score_tile_mma_frag(uint32_t stage, int r0, const MmaWeights<D, G> &w, int blk,
+                                                    float (&o)[4]) {
   constexpr int F = D / 2;
   const int lane = threadIdx.x & 31;
   const int lrow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row of this lane
@@ -275,24 +278,30 @@ __device__ __forceinline__ void score_tile_mma(uint32_t stage, int r0, int nrows
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) acc[e] += accm[e];
-  // D fragment: acc[0..1] row r, columns n, n + 1; acc[2..3] row r + 8.
-  const int r = lane >> 2, n = 2 * (lane & 3);
   if constexpr (G == 8) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int row = r0 + r + (e >> 1) * 8;
-      if (row < nrows) scores[(n + (e & 1)) * sstride + row0 + row] = acc[e];
-    }
+    for (int e = 0; e < 4; ++e) o[e] = acc[e];
   } else {
-    float o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[e] = acc[e] + __shfl_xor_sync(0xffffffffu, acc[e], 2);   // hi + lo
-    if (n < 4) {
+  }
+}
+
+// Scores the 16 keys at stage rows [r0, r0 + 16) (row0 + r0 + i is the key's
+// index in the caller's score rows); rows at or past nrows are not stored.
+template <int D, int G, int TR>
+__device__ __forceinline__ void score_tile_mma(uint32_t stage, int r0, int nrows, int row0, float *scores,
+                                               int sstride, const MmaWeights<D, G> &w, int blk) {
+  const int lane = threadIdx.x & 31;
+  float o[4];
+  score_tile_mma_frag<D, G, TR>(stage, r0, w, blk, o);
+  // D fragment: o[0..1] row r, columns n, n + 1; o[2..3] row r + 8.
+  const int r = lane >> 2, n = 2 * (lane & 3);
+  if (G == 8 || n < 4) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = r0 + r + (e >> 1) * 8, h = n + (e & 1);
-        if (h < G && row < nrows) scores[h * sstride + row0 + row] = o[e];
-      }
+    for (int e = 0; e < 4; ++e) {
+      const int row = r0 + r + (e >> 1) * 8, h = n + (e & 1);
+      if (h < G && row < nrows) scores[h * sstride + row0 + row] = o[e];
     }
   }
 }

@@ -41,7 +41,7 @@ struct CacheView {
   int tm_ok;              // paged, and the block maps (box = one block of one head) are valid
   int g4_ok;              // the row maps (2-D [rows][d], box one row) are valid
 
-  __device__ __forceinline__ bool paged() const { return bt != nullptr; }
+  __host__ __device__ __forceinline__ bool paged() const { return bt != nullptr; }
   // Byte offset of slot i of unit (l, s, g); -1 if the block id is out of range.
   __device__ __forceinline__ long long row_off(int l, int s, int g, int i) const {
     if (bt == nullptr) return ((((long long)l * S + s) * Hkv + g) * cap + i) * (long long)rb;
@@ -885,8 +885,9 @@ __device__ __noinline__ bool compact_unit_runs(const CacheView &c, int l, int s,
 //   - dense caches whose chunk has at most kRunLimit runs of consecutive source
 //     slots: one bulk copy per run;
 //   - otherwise (scattered sources, and every chunk of a paged cache): one
-//     tile::gather4 of 4 source rows per quad of destination rows, through the
-//     row map.
+//     tile::gather4 of 4 source rows per quad of destination rows through the
+//     row map (or, with kCompactLsu = 1, the warp's own 16-byte cp.async
+//     copies, whole rows per instruction).
 // Stores: dense, one bulk store per tensor (the destination rows are
 // contiguous); paged with block maps, one tensor store per destination block
 // (chunks then start at a block boundary: rows below e0 in the first block are
@@ -898,9 +899,19 @@ __device__ __noinline__ bool compact_unit_runs(const CacheView &c, int l, int s,
 // stage is refilled only after the bulk stores that read it finished reading.
 //
 // ring: nstages (2..kMaxCompactStages) stages of kStageBytes; cbars: nstages
-// mbarriers initialised with arrival count 1.  Returns false if a wait timed out
+// mbarriers initialised with arrival count kCompactArrivals.  Returns false if a wait timed out
 // (status recorded; loads already issued are waited for, bounded).
-constexpr int kRunLimit = 8;   // runs per chunk up to which bulk copies beat gather4
+constexpr int kRunLimit = 8;   // runs per chunk up to which bulk copies beat row gathers
+#ifndef TRI_COMPACT_LSU
+#define TRI_COMPACT_LSU 0
+#endif
+// Scattered rows are gathered by tile::gather4 tensor copies (0) or by the
+// warp's own 16-byte cp.async copies (1).  Measured on the long and the paged
+// workloads, the tensor gathers were 2-3 % faster, so they are the default.
+constexpr int kCompactLsu = TRI_COMPACT_LSU;
+// Arrivals per phase of a compaction ring barrier: lane 0's byte-count arrival
+// plus one cp.async-completion arrival from each of the warp's 32 lanes.
+constexpr int kCompactArrivals = 33;
 
 // Compacts one tensor (which = 0: K, 1: V) of unit (l, s, g); the calling warp
 // owns it alone (the two tensors are independent arrays, so a K warp and a V
@@ -944,7 +955,7 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
     const int prev = __shfl_up_sync(0xffffffffu, src, 1);
     const bool boundary = valid && (paged || lane == 0 || !((vmask >> (lane - 1)) & 1u) || prev + 1 != src);
     const unsigned bmask = __ballot_sync(0xffffffffu, boundary);
-    const bool use_runs = !paged && (__popc(bmask) <= kRunLimit || c.g4_ok == 0);
+    const bool use_runs = !paged && (__popc(bmask) <= kRunLimit || (!kCompactLsu && c.g4_ok == 0));
     if (use_runs) {
       // one bulk copy per run [lane, next boundary or invalid lane)
       int end = lane;
@@ -957,6 +968,19 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
       __syncwarp();
       if (boundary)
         bulk_g2s(sk + (long long)lane * rb, base + r2 * rb, (uint32_t)((end - lane) * rb), &cbars[st]);
+    } else if (kCompactLsu) {
+      // 16-byte cp.async pieces, ppr lanes per row and 32 / ppr rows per
+      // instruction, so each instruction reads whole rows (coalesced); the
+      // rows land at their destination positions of the stage
+      if (lane == 0) mbar_arrive_expect_tx(&cbars[st], 0u);
+      const int ppr = rb >> 4, rpi = 32 / ppr;
+      const int sub = lane / ppr, piece = lane - sub * ppr;
+      for (int r0 = 0; r0 < rows; r0 += rpi) {
+        const int row = r0 + sub;
+        const long long rr = __shfl_sync(0xffffffffu, r2, row & 31);
+        if (row < rows && ((vmask >> row) & 1u))
+          cp_async16(sk + (long long)row * rb + piece * 16, base + rr * rb + piece * 16);
+      }
     } else if (c.g4_ok) {
       // one tile::gather4 per quad of destination rows (lanes past `rows`
       // repeat the quad's first valid row; those smem rows are never stored)
@@ -980,6 +1004,8 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
       __syncwarp();
       if (valid) bulk_g2s(sk + (long long)lane * rb, base + r2 * rb, (uint32_t)rb, &cbars[st]);
     }
+    // every lane arrives once its cp.async copies (if any) have landed
+    cp_async_arrive_noinc(&cbars[st]);
   };
 
   for (int x = 0; x < nstages - 1 && x < nch; ++x) issue_loads(x);
@@ -994,6 +1020,8 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
       ok = false;
       break;
     }
+    // rows written by cp.async (generic proxy) are read next by TMA stores
+    fence_proxy_async_smem();
     if (!paged) {
       if (lane == 0) bulk_s2g(base + c.row_off(l, s, g, j0), sk, (uint32_t)(rows * rb));
     } else if (blkst) {
@@ -1016,6 +1044,7 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
     for (int x = cidx; x < nch && x < cidx + nstages - 1; ++x)
       if (!mbar_wait(&cbars[x % nstages], (uint32_t)((x / nstages) & 1))) break;
   }
+  cp_async_wait_all();   // this lane's gathers (global reads: they always complete)
   bulk_wait<0>();
   return ok;
 }

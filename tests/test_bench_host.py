@@ -1,8 +1,8 @@
 """Host-side checks of bench.py that need no GPU.
 
 The bench line names the kernels a step launches; for long units that name
-follows the library's own rule for choosing select2_kernel (its shared-memory
-layout and ring size).  These tests restate that rule from the constants in the
+follows the library's own rule for choosing select_only_kernel +
+compact_only_kernel (the compaction's shared-memory layout and ring size).  These tests restate that rule from the constants in the
 CUDA sources and check bench.py's copy of it, so the two cannot drift apart.
 """
 import os
@@ -27,13 +27,13 @@ def _const(name):
 
 
 def _rule(B, cap, compact):
-    stages, stage, sel_ints, max_smem = (_const("kSel2Stages"), _const("kStageBytes"), _const("kSelInts"),
+    stages, stage, sel_ints, max_smem = (_const("kCoStages"), _const("kStageBytes"), _const("kSelInts"),
                                          _const("kMaxSmem"))
     up = lambda x, a: -(-x // a) * a
     bcap = up(min(B, cap), 32)
-    total = stages * stage + 2 * stages * 8 + 1024 + sel_ints * 4 + 128 + up(bcap * 4, 128)
+    total = stages * stage + 2 * stages * 8 + sel_ints * 4 + up(bcap * 4, 128)
     hf_ok = compact != "holefill" or B + 16 + 4 * max(min(B, cap - B), 0) <= stages * stage
-    return "select2_kernel" if total <= max_smem and hf_ok else "select_compact_kernel"
+    return "select_only_kernel+compact_only_kernel" if total <= max_smem and hf_ok else "select_compact_kernel"
 
 
 @pytest.mark.parametrize("B", [256, 1024, 2048, 8192, 16000, 40000])
