@@ -480,7 +480,7 @@ def _extra(m, compact, steps, warmup, world, local, peak, note):
             "gpu_launches": m.launches * steps, "clocks": clocks}
 
 
-def decode_leg(tk, dev, windows, warmup_windows, world, local, peak):
+def decode_leg(tk, dev, windows, warmup_windows, world, local, peak, layers=None):
     """The decode loop around the step on Qwen3-8B shapes (36 layers, 32/8 heads,
     d = 128, bf16, 16 sequences, paged 16-token blocks, B = 2048): every token
     appends K/V to all units and attends (tri_append_kv + tri_decode_attention
@@ -492,6 +492,8 @@ def decode_leg(tk, dev, windows, warmup_windows, world, local, peak):
     import torch
     from synth import WORKLOADS, generate
     w = WORKLOADS[WORKLOAD].with_(name="decode_loop_qwen3_8b_36l_b16_paged", paged=True, block=16)
+    if layers:
+        w = w.with_(L=layers)
     window, B = 128, w.budget
     data = generate(w, device=dev)                       # 2176 rows per sequence
     cache = tk.KVCache(data["k"], data["v"], torch.full((w.S,), B, dtype=torch.int32, device=dev), Hkv=w.Hkv,
@@ -528,9 +530,11 @@ def decode_leg(tk, dev, windows, warmup_windows, world, local, peak):
     assert tk.tri_get_device_status() == 0
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(windows)]
     with ClockSampler(local) as clk:
+        torch.cuda.nvtx.range_push("timed")
         for e in evs:
             run_window(e)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     assert tk.tri_get_device_status() == 0
     dec_ms = [e[0].elapsed_time(e[1]) for e in evs]
     cmp_ms = [e[1].elapsed_time(e[2]) for e in evs]
@@ -714,7 +718,8 @@ def main():
         import kv_cache_compression_06_b300 as tk
         local = int(os.environ.get("LOCAL_RANK", "0"))
         torch.cuda.set_device(local)
-        res = decode_leg(tk, torch.device("cuda", local), args.decode_windows, 1, 1, local, _peaks()[0])
+        res = decode_leg(tk, torch.device("cuda", local), args.decode_windows, 1, 1, local, _peaks()[0],
+                         layers=args.layers)
         print(json.dumps(res), flush=True)
     else:
         run_b300(args, w)
