@@ -236,11 +236,12 @@ def _select_kernel_name(w, cap, compact):
     select_only_kernel then compact_only_kernel when the compaction's shared
     memory (a 6 x 16 KB ring, 96 barrier bytes, 256 selection bytes, the kept
     list) fits 227 KB and, for hole-fill, the ring holds the hole bookkeeping
-    (B + 16 + 4 min(B, cap - B) bytes); else select_compact_kernel."""
+    (B + 16 + 4 min(B, cap - B) bytes, rounded to 128) and 16 KB of staging;
+    else select_compact_kernel."""
     B = w.budget
     bcap = -(-min(B, cap) // 32) * 32
     total = 6 * 16384 + 2 * 6 * 8 + 256 + -(-bcap * 4 // 128) * 128
-    hf_ok = compact != "holefill" or B + 16 + 4 * max(min(B, cap - B), 0) <= 6 * 16384
+    hf_ok = compact != "holefill" or -(-(B + 16 + 4 * max(min(B, cap - B), 0)) // 128) * 128 + 16384 <= 6 * 16384
     return "select_only_kernel+compact_only_kernel" if total <= 232448 and hf_ok else "select_compact_kernel"
 
 

@@ -132,7 +132,7 @@ struct FusedLayout {
     int o = kRingBytes;
     bars = o;   o += 256;                 // score barriers, 2 x kStages compaction barriers, flags
     wts = o;    o += align_up(G * 3 * F * 4, 128);
-    red = o;    o += 512;
+    red = o;    o += 1024;                // block sums; per-warp moment states, then the merged moments
     hist = o;   o += 1024;
     sm = o;     o += 256;
     scores = o; o += align_up(G * sstride * 4, 128);
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kFusedThreads, (G <= 4 ? 2 : 1)) fused_kernel(
   const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
   const int e0 = build_kept_chunked(keys, N, B, T, ntie, idxs, sm);
   if (a.holefill) {   // keys are dead: their 4N bytes hold the hole-fill bookkeeping
-    holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), sm,
+    holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), ring, kRingBytes, sm,
                   a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
     return;
   }
@@ -268,7 +268,7 @@ struct TileArgs {
   const int *t;
   int budget, skip_small, inter, ntiles, mma_ok;
   long long raw_stride;
-  const float2 *phase;   // [S][F] step phases (phase_kernel)   // floats between the raw rows of two heads (cap, or capp in the workspace)
+  const float2 *phase;   // [S][F] step phases (phase_kernel); raw_stride: floats between the raw rows of two heads (cap, or capp in the workspace)
   float *raw;      // [(u*G + h)*raw_stride + i]
   float2 *part;    // [(u*ntiles + tile)*G + h] = (mean, M2) of the tile
   StepConst sc;
@@ -550,6 +550,87 @@ __global__ void __launch_bounds__(kThreads, 2) score_tiles_mma_kernel(const __gr
   }
 }
 
+// Chan's combination of (count, mean, M2) summaries: (n, mean, M2) absorbs (nb, mb, Mb).
+__device__ __forceinline__ void chan_merge(float &n, float &mean, float &M2, float nb, float mb, float Mb) {
+  if (nb <= 0.f) return;
+  if (n <= 0.f) {
+    n = nb;
+    mean = mb;
+    M2 = Mb;
+    return;
+  }
+  const float tot = n + nb, dl = mb - mean;
+  mean = fmaf(dl, nb / tot, mean);
+  M2 = M2 + Mb + dl * dl * (n * nb / tot);
+  n = tot;
+}
+
+// ---------------------------------------------------------------- moments from MMA fragments
+// Per-lane shifted sums of the scores of the two heads n0, n0 + 1 (n0 = 2 (lane
+// % 4)) that a lane holds in the m16n8 fragments: the shift is the first score
+// the lane sees, so a constant head has exactly zero deviation.
+struct LaneMoments {
+  float cnt = 0.f, sh[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f}, s2[2] = {0.f, 0.f};
+  __device__ __forceinline__ void add(float x0, float x1) {
+    if (cnt == 0.f) {
+      sh[0] = x0;
+      sh[1] = x1;
+    }
+    const float d0 = x0 - sh[0], d1 = x1 - sh[1];
+    s1[0] += d0;
+    s1[1] += d1;
+    s2[0] = fmaf(d0, d0, s2[0]);
+    s2[1] = fmaf(d1, d1, s2[1]);
+    cnt += 1.f;
+  }
+  // (count, mean, M2) of the warp's lanes of this lane's class, merged (Chan)
+  // over lane bits 2..4; lanes 0..3 write theirs to red[(warp * 4 + lane) * 5 ..].
+  __device__ __forceinline__ void to_shared(float *red, int warp) const {
+    const int lane = threadIdx.x & 31;
+    float n = cnt, mean[2], m2[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      mean[j] = n > 0.f ? sh[j] + s1[j] / n : 0.f;
+      m2[j] = n > 0.f ? fmaxf(s2[j] - s1[j] * s1[j] / n, 0.f) : 0.f;
+    }
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+      const float nb = __shfl_xor_sync(0xffffffffu, n, off);
+      float mb[2], qb[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        mb[j] = __shfl_xor_sync(0xffffffffu, mean[j], off);
+        qb[j] = __shfl_xor_sync(0xffffffffu, m2[j], off);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float nn = n;
+        chan_merge(nn, mean[j], m2[j], nb, mb[j], qb[j]);
+      }
+      n += nb;
+    }
+    if (lane < 4) {
+      float *rw = red + (warp * 4 + lane) * 5;
+      rw[0] = n;
+      rw[1] = mean[0];
+      rw[2] = mean[1];
+      rw[3] = m2[0];
+      rw[4] = m2[1];
+    }
+  }
+};
+
+// Merges the nwarps warps' states in red for head h: (count, mean, M2).
+__device__ __forceinline__ void merge_warp_moments(const float *red, int nwarps, int h, float &n, float &mean,
+                                                   float &m2) {
+  const int cls = h / 2, j = h & 1;
+  n = mean = m2 = 0.f;
+  for (int wp = 0; wp < nwarps; ++wp) {
+    const float *rw = red + (wp * 4 + cls) * 5;
+    chan_merge(n, mean, m2, rw[0], rw[1 + j], rw[3 + j]);
+  }
+}
+
 // ---------------------------------------------------------------- fused short-unit kernel, tensor cores
 // fused_kernel with the tensor-core score of score_tiles_mma_kernel (bf16
 // caches, rotate-half bands): a producer warp streams the unit's K through the
@@ -644,14 +725,29 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
     load_mma_weights<D, G>(w, wts, kConsumerWarps * 32, warp == 0);
     const int grp = warp / SPS, sub = warp % SPS;
     const uint32_t ring_a = smem_u32(ring);
+    // fragment geometry: this lane holds keys r, r + 8 of a tile for heads n0, n0 + 1
+    const int r = lane >> 2, n0 = 2 * (lane & 3);
+    const bool holds = G == 8 || n0 < G;
+    LaneMoments lm;
     for (int t = grp; t < nst; t += GROUPS) {
       const int st = t % kStages;
       if (!*pipe.fail && !mbar_wait(&pipe.full[st], (uint32_t)((t / kStages) & 1))) *pipe.fail = 1;
-      score_tile_mma<D, G, TR>(ring_a + st * kStageBytes, 16 * sub, min(TR, N - t * TR), t * TR, scores, ss, w,
-                               c.paged() ? c.block : 0);
+      float o[4];
+      score_tile_mma_frag<D, G, TR>(ring_a + st * kStageBytes, 16 * sub, w, c.paged() ? c.block : 0, o);
       __syncwarp();
       if (lane == 0) mbar_arrive(&pipe.empty[st]);
+      const int nrows = min(TR, N - t * TR), row0 = t * TR;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int row = 16 * sub + r + 8 * hh;
+        if (holds && row < nrows) {
+          scores[n0 * ss + row0 + row] = o[2 * hh];
+          if (G > 1) scores[(n0 + 1) * ss + row0 + row] = o[2 * hh + 1];
+          lm.add(o[2 * hh], o[2 * hh + 1]);
+        }
+      }
     }
+    lm.to_shared(red, warp);
   }
   __syncthreads();
   if (*pipe.fail) {
@@ -665,8 +761,22 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
     return;
   }
 
+  // the heads' moments from the consumer warps' states
+  float *mom = red + kConsumerWarps * 4 * 5;
+  if (tid < G) {
+    float n, mean, m2;
+    merge_warp_moments(red, kConsumerWarps, tid, n, mean, m2);
+    const float sd = sqrtf(m2 / (float)N);
+    mom[tid] = mean;
+    mom[8 + tid] = sd > 0.f ? 1.0f / sd : 0.0f;
+  }
+  __syncthreads();
   float mu[G], inv[G];
-  head_moments<G>(scores, ss, N, red, mu, inv);
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    mu[h] = mom[h];
+    inv[h] = mom[8 + h];
+  }
   uint32_t *keys = reinterpret_cast<uint32_t *>(scores);   // overlays head 0's scores
   for (int i = tid; i < N; i += nt) {
     float sv[G];
@@ -691,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
   const int e0 = build_kept_chunked(keys, N, B, T, ntie, idxs, sm);
   if (a.holefill) {
-    holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), sm,
+    holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), ring, kRingBytes, sm,
                   a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
     return;
   }
@@ -705,21 +815,6 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   } else {
     if (warp == 0) compact_unit_runs(c, l, s, g, idxs, e0, B, N, ring, cbars);
   }
-}
-
-// Chan's combination of (count, mean, M2) summaries: (n, mean, M2) absorbs (nb, mb, Mb).
-__device__ __forceinline__ void chan_merge(float &n, float &mean, float &M2, float nb, float mb, float Mb) {
-  if (nb <= 0.f) return;
-  if (n <= 0.f) {
-    n = nb;
-    mean = mb;
-    M2 = Mb;
-    return;
-  }
-  const float tot = n + nb, dl = mb - mean;
-  mean = fmaf(dl, nb / tot, mean);
-  M2 = M2 + Mb + dl * dl * (n * nb / tot);
-  n = tot;
 }
 
 // Merges the per-tile (mean, M2) of a unit's N keys; warp h < G handles head h
@@ -757,6 +852,43 @@ __device__ __forceinline__ void merge_tile_moments(const float2 *part, long long
     const float sd = sqrtf(M2 / n);
     mom[h] = mean;
     mom[8 + h] = sd > 0.f ? 1.0f / sd : 0.0f;
+  }
+}
+
+// a3 from key-major raw scores: key i's G scores are raw_u[i*G .. i*G + G)
+// (16-byte aligned rows of 4 keys); each thread takes quads of keys (G 16-byte
+// loads, contiguous across threads) and writes their order-preserving keys.
+// Key slots in [N, round4(N)) receive don't-care values.
+template <int G>
+__device__ void zmax_from_raw_km(const float *raw_u, int N, const float *mom, uint32_t *keys) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  float mu[G], iv[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    mu[h] = mom[h];
+    iv[h] = mom[8 + h];
+  }
+  const int n4 = (N + 3) / 4;
+  const float4 *rows = reinterpret_cast<const float4 *>(raw_u);
+  for (int q = tid; q < n4; q += nt) {
+    float x[4 * G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const float4 v = __ldg(rows + (long long)q * G + k);
+      x[4 * k] = v.x;
+      x[4 * k + 1] = v.y;
+      x[4 * k + 2] = v.z;
+      x[4 * k + 3] = v.w;
+    }
+    uint32_t kk[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float z = (x[j * G] - mu[0]) * iv[0];
+#pragma unroll
+      for (int h = 1; h < G; ++h) z = fmaxf(z, (x[j * G + h] - mu[h]) * iv[h]);
+      kk[j] = score_key(z);
+    }
+    reinterpret_cast<uint4 *>(keys)[q] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
   }
 }
 
@@ -832,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 2) score_keys_mma_kernel(const __gri
   // lane state: shifted sums of the two heads n0, n0 + 1 of this lane
   const int r = lane >> 2, n0 = 2 * (lane & 3);
   const bool holds = G == 8 || n0 < G;
-  float cnt = 0.f, sh[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f}, s2[2] = {0.f, 0.f};
+  LaneMoments lm;
   if (warp == kProducerWarp) {
     int t = 0;
     for (; t < nst; ++t) {
@@ -870,51 +1002,11 @@ __global__ void __launch_bounds__(kThreads, 2) score_keys_mma_kernel(const __gri
             raw_c[key] = x0;
           else
             *reinterpret_cast<float2 *>(raw_c + (long long)key * G + n0) = make_float2(x0, x1);
-          if (cnt == 0.f) {
-            sh[0] = x0;
-            sh[1] = x1;
-          }
-          const float d0 = x0 - sh[0], d1 = x1 - sh[1];
-          s1[0] += d0;
-          s1[1] += d1;
-          s2[0] = fmaf(d0, d0, s2[0]);
-          s2[1] = fmaf(d1, d1, s2[1]);
-          cnt += 1.f;
+          lm.add(x0, x1);
         }
       }
     }
-    // this lane's (count, mean, M2) per head slot, merged over the lanes of
-    // the same class (lane % 4: same heads), then written per warp
-    float mean[2], m2[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      mean[j] = cnt > 0.f ? sh[j] + s1[j] / cnt : 0.f;
-      m2[j] = cnt > 0.f ? fmaxf(s2[j] - s1[j] * s1[j] / cnt, 0.f) : 0.f;
-    }
-#pragma unroll
-    for (int off = 4; off <= 16; off <<= 1) {
-      const float nb = __shfl_xor_sync(0xffffffffu, cnt, off);
-      float mb[2], qb[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        mb[j] = __shfl_xor_sync(0xffffffffu, mean[j], off);
-        qb[j] = __shfl_xor_sync(0xffffffffu, m2[j], off);
-      }
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float nn = cnt;
-        chan_merge(nn, mean[j], m2[j], nb, mb[j], qb[j]);
-      }
-      cnt += nb;
-    }
-    if (lane < 4) {
-      float *rw = red + (warp * 4 + lane) * 5;
-      rw[0] = cnt;
-      rw[1] = mean[0];
-      rw[2] = mean[1];
-      rw[3] = m2[0];
-      rw[4] = m2[1];
-    }
+    lm.to_shared(red, warp);
   }
   __syncthreads();
   if (*fail) {
@@ -928,12 +1020,8 @@ __global__ void __launch_bounds__(kThreads, 2) score_keys_mma_kernel(const __gri
     return;
   }
   if (tid < G) {
-    const int cls = tid / 2, j = tid & 1;
-    float nn = 0.f, mm = 0.f, qq = 0.f;
-    for (int wp = 0; wp < kConsumerWarps; ++wp) {
-      const float *rw = red + (wp * 4 + cls) * 5;
-      chan_merge(nn, mm, qq, rw[0], rw[1 + j], rw[3 + j]);
-    }
+    float nn, mm, qq;
+    merge_warp_moments(red, kConsumerWarps, tid, nn, mm, qq);
     a.part[((long long)u * a.ntiles + blockIdx.x) * G + tid] = make_float2(mm, qq);
   }
 }
@@ -1072,43 +1160,6 @@ __device__ void zmax_from_raw(const float *raw_u, int capp, int N, const float *
   }
 }
 
-// a3 from key-major raw scores: key i's G scores are raw_u[i*G .. i*G + G)
-// (16-byte aligned rows of 4 keys); each thread takes quads of keys (G 16-byte
-// loads, contiguous across threads) and writes their order-preserving keys.
-// Key slots in [N, round4(N)) receive don't-care values.
-template <int G>
-__device__ void zmax_from_raw_km(const float *raw_u, int N, const float *mom, uint32_t *keys) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  float mu[G], iv[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    mu[h] = mom[h];
-    iv[h] = mom[8 + h];
-  }
-  const int n4 = (N + 3) / 4;
-  const float4 *rows = reinterpret_cast<const float4 *>(raw_u);
-  for (int q = tid; q < n4; q += nt) {
-    float x[4 * G];
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-      const float4 v = __ldg(rows + (long long)q * G + k);
-      x[4 * k] = v.x;
-      x[4 * k + 1] = v.y;
-      x[4 * k + 2] = v.z;
-      x[4 * k + 3] = v.w;
-    }
-    uint32_t kk[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float z = (x[j * G] - mu[0]) * iv[0];
-#pragma unroll
-      for (int h = 1; h < G; ++h) z = fmaxf(z, (x[j * G + h] - mu[h]) * iv[h]);
-      kk[j] = score_key(z);
-    }
-    reinterpret_cast<uint4 *>(keys)[q] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
-  }
-}
-
 // zmax_from_raw or zmax_from_raw_km for the unit's G.
 template <bool PF>
 __device__ __forceinline__ void zmax_dispatch(const SCArgs &a, long long u, int N, const float *mom,
@@ -1186,7 +1237,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
       return;
     }
     if (a.holefill) {
-      holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), sm, nullptr);
+      const int wb = align_up(holefill_work_bytes(B, N), 128);
+      holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys) + lay.bars - wb, reinterpret_cast<char *>(keys),
+                    lay.bars - wb, sm, nullptr);
       return;
     }
     for (int j = tid; j < B; j += nt)
@@ -1211,8 +1264,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_compact_kernel(const __
   const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
   const int e0 = build_kept(keys, N, B, T, ntie, idxs, sm);
   if (a.mode == 0 && a.holefill) {   // keys are dead: their region holds the hole-fill bookkeeping
-    holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), sm,
-                  a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
+    const int wb = align_up(holefill_work_bytes(B, N), 128);
+    holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys) + lay.bars - wb, reinterpret_cast<char *>(keys),
+                  lay.bars - wb, sm, a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
     return;
   }
   if (a.idx_out != nullptr)
@@ -1256,19 +1310,11 @@ __global__ void __launch_bounds__(kSelOnlyThreads) select_only_kernel(const __gr
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
-  const bool len_writer = tid == 0 && a.new_len != nullptr && l == 0 && g == 0;
-  if (N <= B) {
-    if (len_writer) a.new_len[s] = N;
-    if (a.idx_out != nullptr)
-      for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = j < N ? j : -1;
+  (void)nt;
+  if (N <= B) return;            // compact_only_kernel writes its outputs
+  if (!c.blocks_ok(s, N)) {      // the sequence is skipped (status recorded by compact_only_kernel)
     return;
   }
-  if (!c.blocks_ok(s, N)) {   // the sequence is skipped: its length stays N
-    if (tid == 0) set_status(TRI_ERR_BOUNDS);
-    if (len_writer) a.new_len[s] = N;
-    return;
-  }
-  if (len_writer) a.new_len[s] = B;
   merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom, a.part_keys);
   __syncthreads();
   uint32_t *keys = a.keys + (long long)u * a.capp;
@@ -1305,9 +1351,24 @@ __global__ void __launch_bounds__(kCoThreads, 2) compact_only_kernel(const __gri
   if (timed_out()) return;
   const int N = c.seq_len[s];
   const int B = a.budget;
-  // units the selection left alone (N <= B, N > cap, bad block ids) are left alone here too
-  if (N <= B || N > c.cap) return;
-  if (!c.blocks_ok(s, N)) return;
+  if (N < 0 || N > c.cap) {
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  // the new lengths and, for units with N <= B, the identity indices
+  const bool len_writer = tid == 0 && a.new_len != nullptr && l == 0 && g == 0;
+  if (N <= B) {
+    if (len_writer) a.new_len[s] = N;
+    if (a.idx_out != nullptr)
+      for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = j < N ? j : -1;
+    return;
+  }
+  if (!c.blocks_ok(s, N)) {   // the sequence is skipped: its length stays N
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    if (len_writer) a.new_len[s] = N;
+    return;
+  }
+  if (len_writer) a.new_len[s] = B;
   if (tid == 0) {
     for (int st = 0; st < kCoStages; ++st) {
       mbar_init(&cbars[st], kCompactArrivals);               // K warp
@@ -1320,7 +1381,9 @@ __global__ void __launch_bounds__(kCoThreads, 2) compact_only_kernel(const __gri
   const int e0 = a.e0s[u];
   __syncthreads();
   if (a.holefill) {
-    holefill_unit(c, l, s, g, idxs, B, N, ring, sm, a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
+    const int wb = align_up(holefill_work_bytes(B, N), 128);
+    holefill_unit(c, l, s, g, idxs, B, N, ring + kCoStages * kStageBytes - wb, ring, kCoStages * kStageBytes - wb, sm,
+                  a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
     return;
   }
   if ((tid >> 5) < 2)
@@ -2010,30 +2073,35 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
     sa.part_keys = tile_keys_for(G);
   }
   sa.ntiles = ta.ntiles;
-  if ((e = run_phases(cache, ta, stream)) != TRI_OK) return e;
-  if ((e = TRI_DISPATCH(run_keys, cache->d, G, bf16, ta, units, stream)) != TRI_OK) return e;
   sa.raw = ta.raw;
   sa.part = ta.part;
   sa.idx_out = idx_out;
   sa.new_len = new_len;
-  sa.keys = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + w.keys_off);
+  char *wsb = static_cast<char *>(ws);
+  sa.keys = reinterpret_cast<uint32_t *>(wsb + w.keys_off);
   // selection, then compaction (two kernels), when the compaction's ring holds
-  // the hole-fill bookkeeping (B bytes + 4 min(B, N - B)) and its shared memory
-  // the kept list; else the one-per-SM kernel with keys in shared memory
+  // the hole-fill bookkeeping (B bytes + 4 min(B, N - B)) with room to stage
+  // rows and its shared memory the kept list; else the one-per-SM kernel with
+  // keys in shared memory.
   const CoLayout co(sa.bcap);
   const int64_t movers = std::min<int64_t>(params->budget, cache->cap - params->budget);
-  const bool hf_fits = !sa.holefill || params->budget + 16 + 4 * std::max<int64_t>(movers, 0) <= kCoStages * kStageBytes;
-  if (co.total <= kMaxSmem && hf_fits) {
-    char *wsb = static_cast<char *>(ws);
+  // hole-fill: the bookkeeping sits at the end of the ring, and at least 16 KB
+  // stays for staging the moved rows
+  const bool hf_fits = !sa.holefill || align_up(params->budget + 16 + 4 * (int)std::max<int64_t>(movers, 0), 128) +
+                                               16384 <= kCoStages * kStageBytes;
+  const bool split = co.total <= kMaxSmem && hf_fits;
+  if (split) {
     sa.kept = (!sa.holefill && idx_out != nullptr) ? idx_out : reinterpret_cast<int *>(wsb + w.kept_off);
     sa.e0s = reinterpret_cast<int *>(wsb + w.e0_off);
-    select_only_kernel<<<(unsigned)units, kSelOnlyThreads, 0, stream>>>(sa);
-    if ((e = launch_result()) != TRI_OK) return e;
-    if (set_smem(compact_only_kernel, co.total) != TRI_OK) return TRI_ERR_CUDA;
-    compact_only_kernel<<<(unsigned)units, kCoThreads, co.total, stream>>>(sa);
-    return launch_result();
   }
-  return run_select_compact(sa, units, stream);
+  if ((e = run_phases(cache, ta, stream)) != TRI_OK) return e;
+  if ((e = TRI_DISPATCH(run_keys, cache->d, G, bf16, ta, units, stream)) != TRI_OK) return e;
+  if (!split) return run_select_compact(sa, units, stream);
+  select_only_kernel<<<(unsigned)units, kSelOnlyThreads, 0, stream>>>(sa);
+  if ((e = launch_result()) != TRI_OK) return e;
+  if (set_smem(compact_only_kernel, co.total) != TRI_OK) return TRI_ERR_CUDA;
+  compact_only_kernel<<<(unsigned)units, kCoThreads, co.total, stream>>>(sa);
+  return launch_result();
 }
 
 tri_status tri_compress_step_static_scratch(const tri_cache *cache, const tri_stats *stats,

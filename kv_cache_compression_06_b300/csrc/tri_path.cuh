@@ -1050,17 +1050,28 @@ __device__ __noinline__ bool compact_unit_tma(const CacheView &c, const TmaMaps 
 }
 
 // ---------------------------------------------------------------- hole-fill compaction (a5, alternative)
+// Bytes of holefill_unit's bookkeeping for a unit of N keys: one flag byte per
+// slot below B (rounded to 16), then the hole list (at most min(B, N - B) ints).
+__host__ __device__ __forceinline__ int holefill_work_bytes(int B, int N) {
+  const int movers = N - B < B ? N - B : B;
+  return ((B + 15) & ~15) + 4 * (movers > 0 ? movers : 0);
+}
+
 // Hole-fill layout of unit (l, s, g) from its ascending kept list idx[0..B):
 // kept slots below B stay; the evicted slots below B (holes, ascending) receive
 // the kept slots at or above B (movers, ascending), the k-th hole the k-th
 // mover.  Sources (>= B) and destinations (< B) are disjoint, so every row copy
-// is independent: all threads of the CTA copy 16-byte pieces, four loads in
-// flight per thread before their stores.  `work` (shared, >= 4 N bytes, 16-byte
-// aligned, dead by now) holds one flag byte per slot below B, then the hole
-// list.  out (global, may be null) receives the layout: out[j] = original slot
-// now at j.  sm: 40 ints for the scan.  Ends with a CTA barrier.
+// is independent.  The movers' K and V rows are gathered with 16-byte
+// cp.async copies (a warp per row, its lanes on the row's pieces) into
+// `stage` in batches that fill half of it, the next batch in flight while the
+// current one is stored from shared memory to its holes.  `work` (shared,
+// holefill_work_bytes(B, N), 16-byte aligned, dead by now, disjoint from
+// `stage`) holds one flag byte per slot below B, then the hole list.  stage:
+// 16-byte aligned; with less than 4 row sizes the rows are copied directly.  out (global, may be null)
+// receives the layout: out[j] = original slot now at j.  sm: 40 ints for the
+// scan.  Ends with a CTA barrier.
 __device__ __noinline__ void holefill_unit(const CacheView &c, int l, int s, int g, const int *idx, int B,
-                                           int N, char *work, int *sm, int *out) {
+                                           int N, char *work, char *stage, int stage_bytes, int *sm, int *out) {
   const int tid = threadIdx.x, nt = blockDim.x;
   unsigned char *kept = reinterpret_cast<unsigned char *>(work);
   int *holes = reinterpret_cast<int *>(work + ((B + 15) & ~15));
@@ -1089,33 +1100,68 @@ __device__ __noinline__ void holefill_unit(const CacheView &c, int l, int s, int
     }
   }
   __syncthreads();
-  // copy mover rows into the holes (K and V): piece q of the 2 * ppr pieces of
-  // pair k (ppr = 16-byte pieces per row, a power of two) is K piece q for
-  // q < ppr, else V piece q - ppr; each lane keeps 4 pieces in flight
-  const int ppr = c.rb / 16, lp = __ffs(2 * ppr) - 1;
+  // copy mover k's K and V rows into hole k, in batches of `rh` movers per
+  // half of the stage.  A warp owns a row at a time (its source and
+  // destination offsets computed once), its lanes take the row's 2 ppr
+  // 16-byte pieces (K pieces, then V pieces).
+  const int rb = c.rb, ppr = rb >> 4, pp = 2 * ppr;
   const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  const int pieces = total << lp;
-  for (int base = warp * 128; base < pieces; base += nw * 128) {
-    uint4 v[4];
-    char *dst[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int q = base + e * 32 + lane;
-      dst[e] = nullptr;
-      if (q < pieces) {
-        const int k = q >> lp, rem = q & (2 * ppr - 1);
-        const int tsr = rem >= ppr, col = rem & (ppr - 1);
-        char *tb = tsr ? c.v : c.k;
-        const long long so = c.row_off(l, s, g, idx[P + k]), dof = c.row_off(l, s, g, holes[k]);
-        if (so >= 0 && dof >= 0) {
-          v[e] = *reinterpret_cast<const uint4 *>(tb + so + col * 16);
-          dst[e] = tb + dof + col * 16;
-        }
+  const int rh = stage_bytes / (4 * rb);
+  if (rh < 1) {
+    // no room to stage: 16-byte copies straight from the movers to the holes
+    for (int k = warp; k < total; k += nw) {
+      const long long so = c.row_off(l, s, g, idx[P + k]), dof = c.row_off(l, s, g, holes[k]);
+      if (so < 0 || dof < 0) continue;
+      for (int q = lane; q < pp; q += 32) {
+        char *base = q < ppr ? c.k : c.v;
+        const int col = (q < ppr ? q : q - ppr) * 16;
+        *reinterpret_cast<uint4 *>(base + dof + col) = *reinterpret_cast<const uint4 *>(base + so + col);
       }
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (dst[e] != nullptr) *reinterpret_cast<uint4 *>(dst[e]) = v[e];
+    __syncthreads();
+    return;
+  }
+  const int nbat = (total + rh - 1) / rh;
+  const int half = rh * 2 * rb;
+  auto issue = [&](int b) {
+    char *st = stage + (b & 1) * half;
+    const int k0 = b * rh, nr = min(rh, total - k0);
+    for (int k = warp; k < nr; k += nw) {
+      const long long so = c.row_off(l, s, g, idx[P + k0 + k]);
+      if (so < 0) continue;
+      for (int q = lane; q < pp; q += 32) {
+        const char *base = q < ppr ? c.k : c.v;
+        const int col = (q < ppr ? q : q - ppr) * 16;
+        cp_async16(st + (long long)k * 2 * rb + (q < ppr ? 0 : rb) + col, base + so + col);
+      }
+    }
+    cp_async_commit();
+  };
+  auto store = [&](int b) {
+    const char *st = stage + (b & 1) * half;
+    const int k0 = b * rh, nr = min(rh, total - k0);
+    for (int k = warp; k < nr; k += nw) {
+      const long long so = c.row_off(l, s, g, idx[P + k0 + k]), dof = c.row_off(l, s, g, holes[k0 + k]);
+      if (so < 0 || dof < 0) continue;
+      for (int q = lane; q < pp; q += 32) {
+        char *base = q < ppr ? c.k : c.v;
+        const int col = (q < ppr ? q : q - ppr) * 16;
+        *reinterpret_cast<uint4 *>(base + dof + col) =
+            *reinterpret_cast<const uint4 *>(st + (long long)k * 2 * rb + (q < ppr ? 0 : rb) + col);
+      }
+    }
+  };
+  if (nbat > 0) issue(0);
+  for (int b = 0; b < nbat; ++b) {
+    if (b + 1 < nbat) {
+      issue(b + 1);           // its half was freed by the barrier that ended batch b - 1
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();          // batch b has landed for every thread
+    store(b);
+    __syncthreads();          // batch b's half may be refilled
   }
   __syncthreads();
 }

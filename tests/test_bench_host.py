@@ -32,7 +32,7 @@ def _rule(B, cap, compact):
     up = lambda x, a: -(-x // a) * a
     bcap = up(min(B, cap), 32)
     total = stages * stage + 2 * stages * 8 + sel_ints * 4 + up(bcap * 4, 128)
-    hf_ok = compact != "holefill" or B + 16 + 4 * max(min(B, cap - B), 0) <= stages * stage
+    hf_ok = compact != "holefill" or up(B + 16 + 4 * max(min(B, cap - B), 0), 128) + 16384 <= stages * stage
     return "select_only_kernel+compact_only_kernel" if total <= max_smem and hf_ok else "select_compact_kernel"
 
 
