@@ -9,8 +9,9 @@ before every step (untimed; the 5.1 GB copy also flushes the 126 MB L2).
 
 The same run also times, each in its own timed region with its own clock
 record and algorithmic bytes ("extras"): the hole-fill layout on the same
-workload, the long 32k-key workload (36 layers x 4 sequences) and a layer group
-of the paged Qwen3-32B-shaped workload (its 64 layers do not fit HBM).
+workload, the long 32k-key workload (36 layers x 4 sequences, both layouts), a
+layer group of the paged Qwen3-32B-shaped workload (its 64 layers do not fit
+HBM) and the decode loop around the step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
 
@@ -625,6 +626,8 @@ def run_b300(args, w):
         m = Measured(tk, WORKLOADS["qwen3_8b_36l_b4_n32768"], dev)
         extras["qwen3_8b_36l_b4_n32768"] = _extra(m, "ordered", args.extra_steps, args.warmup, world, local, peak,
                                                   "long one-shot compression, 32768 -> 2048 keys")
+        extras["qwen3_8b_36l_b4_n32768/holefill"] = _extra(m, "holefill", args.extra_steps, args.warmup, world,
+                                                           local, peak, "same cache and step, hole-fill layout")
         m.free()
         pw = WORKLOADS["qwen3_32b_64l_b64_paged"]
         m = Measured(tk, pw.with_(L=args.paged_layers), dev)

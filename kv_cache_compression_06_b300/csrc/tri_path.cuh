@@ -1061,10 +1061,12 @@ __host__ __device__ __forceinline__ int holefill_work_bytes(int B, int N) {
 // kept slots below B stay; the evicted slots below B (holes, ascending) receive
 // the kept slots at or above B (movers, ascending), the k-th hole the k-th
 // mover.  Sources (>= B) and destinations (< B) are disjoint, so every row copy
-// is independent.  The movers' K and V rows are gathered with 16-byte
-// cp.async copies (a warp per row, its lanes on the row's pieces) into
-// `stage` in batches that fill half of it, the next batch in flight while the
-// current one is stored from shared memory to its holes.  `work` (shared,
+// is independent.  The movers are the tail of the ascending kept list, so
+// their K and V rows are gathered first, with 16-byte cp.async copies (a warp
+// per row, its lanes on the row's pieces) into `stage`, while the holes are
+// ranked; then stored from shared memory to their holes.  All at once when
+// they fit the stage, else in batches of a quarter of it, three in flight
+// while the oldest is stored.  `work` (shared,
 // holefill_work_bytes(B, N), 16-byte aligned, dead by now, disjoint from
 // `stage`) holds one flag byte per slot below B, then the hole list.  stage:
 // 16-byte aligned; with less than 4 row sizes the rows are copied directly.  out (global, may be null)
@@ -1073,23 +1075,58 @@ __host__ __device__ __forceinline__ int holefill_work_bytes(int B, int N) {
 __device__ __noinline__ void holefill_unit(const CacheView &c, int l, int s, int g, const int *idx, int B,
                                            int N, char *work, char *stage, int stage_bytes, int *sm, int *out) {
   const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  const int rb = c.rb, ppr = rb >> 4, pp = 2 * ppr;
+  // the movers (kept slots >= B) are the tail idx[P..B) of the ascending kept
+  // list: their gathers start now, ahead of the bookkeeping
+  int lo = 0, hi = B;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (idx[mid] < B) lo = mid + 1; else hi = mid;
+  }
+  const int P = lo, total = B - P;
+  // every mover fits the stage at once, or batches of a quarter of it cycle
+  // through 4 buffers with 3 batches in flight
+  constexpr int kBufs = 4;
+  const int rows_full = stage_bytes / (2 * rb);
+  const bool single = total <= rows_full;
+  const int rh = single ? rows_full : stage_bytes / (kBufs * 2 * rb);
+  const int half = rh * 2 * rb;   // bytes of one buffer
+  const int nbat = rh > 0 ? (total + rh - 1) / rh : 0;
+  auto issue = [&](int b) {       // always commits a group (empty past the last batch)
+    char *st = stage + (b % kBufs) * half;
+    const int k0 = b * rh, nr = b < nbat ? min(rh, total - k0) : 0;
+    for (int k = warp; k < nr; k += nw) {
+      const long long so = c.row_off(l, s, g, idx[P + k0 + k]);
+      if (so < 0) continue;
+      for (int q = lane; q < pp; q += 32) {
+        const char *base = q < ppr ? c.k : c.v;
+        const int col = (q < ppr ? q : q - ppr) * 16;
+        cp_async16(st + (long long)k * 2 * rb + (q < ppr ? 0 : rb) + col, base + so + col);
+      }
+    }
+    cp_async_commit();
+  };
+  if (rh > 0) {
+    if (single) {
+      if (nbat > 0) issue(0);
+    } else {
+      for (int b = 0; b < kBufs - 1; ++b) issue(b);
+    }
+  }
   unsigned char *kept = reinterpret_cast<unsigned char *>(work);
   int *holes = reinterpret_cast<int *>(work + ((B + 15) & ~15));
   for (int j = tid; j < B; j += nt) kept[j] = 0;
   __syncthreads();
-  for (int j = tid; j < B; j += nt) {
-    const int v = idx[j];
-    if (v < B) kept[v] = 1;
-  }
+  for (int j = tid; j < P; j += nt) kept[idx[j]] = 1;
   __syncthreads();
   // holes in slot order: each thread scans a contiguous chunk of slots
   const int chunk = (B + nt - 1) / nt;
   const int j0 = min(B, tid * chunk), j1 = min(B, j0 + chunk);
   int nh = 0;
   for (int j = j0; j < j1; ++j) nh += kept[j] == 0;
-  int total;
-  int r = block_excl_scan(nh, sm, &total);
-  const int P = B - total;   // kept slots below B; movers are idx[P..B)
+  int nholes;
+  int r = block_excl_scan(nh, sm, &nholes);   // nholes == total
   for (int j = j0; j < j1; ++j) {
     if (kept[j]) {
       if (out != nullptr) out[j] = j;
@@ -1100,13 +1137,8 @@ __device__ __noinline__ void holefill_unit(const CacheView &c, int l, int s, int
     }
   }
   __syncthreads();
-  // copy mover k's K and V rows into hole k, in batches of `rh` movers per
-  // half of the stage.  A warp owns a row at a time (its source and
-  // destination offsets computed once), its lanes take the row's 2 ppr
-  // 16-byte pieces (K pieces, then V pieces).
-  const int rb = c.rb, ppr = rb >> 4, pp = 2 * ppr;
-  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  const int rh = stage_bytes / (4 * rb);
+  // copy mover k's K and V rows into hole k: a warp owns a row at a time, its
+  // lanes take the row's 2 ppr 16-byte pieces (K pieces, then V pieces)
   if (rh < 1) {
     // no room to stage: 16-byte copies straight from the movers to the holes
     for (int k = warp; k < total; k += nw) {
@@ -1121,24 +1153,8 @@ __device__ __noinline__ void holefill_unit(const CacheView &c, int l, int s, int
     __syncthreads();
     return;
   }
-  const int nbat = (total + rh - 1) / rh;
-  const int half = rh * 2 * rb;
-  auto issue = [&](int b) {
-    char *st = stage + (b & 1) * half;
-    const int k0 = b * rh, nr = min(rh, total - k0);
-    for (int k = warp; k < nr; k += nw) {
-      const long long so = c.row_off(l, s, g, idx[P + k0 + k]);
-      if (so < 0) continue;
-      for (int q = lane; q < pp; q += 32) {
-        const char *base = q < ppr ? c.k : c.v;
-        const int col = (q < ppr ? q : q - ppr) * 16;
-        cp_async16(st + (long long)k * 2 * rb + (q < ppr ? 0 : rb) + col, base + so + col);
-      }
-    }
-    cp_async_commit();
-  };
   auto store = [&](int b) {
-    const char *st = stage + (b & 1) * half;
+    const char *st = stage + (b % kBufs) * half;
     const int k0 = b * rh, nr = min(rh, total - k0);
     for (int k = warp; k < nr; k += nw) {
       const long long so = c.row_off(l, s, g, idx[P + k0 + k]), dof = c.row_off(l, s, g, holes[k0 + k]);
@@ -1151,17 +1167,19 @@ __device__ __noinline__ void holefill_unit(const CacheView &c, int l, int s, int
       }
     }
   };
-  if (nbat > 0) issue(0);
-  for (int b = 0; b < nbat; ++b) {
-    if (b + 1 < nbat) {
-      issue(b + 1);           // its half was freed by the barrier that ended batch b - 1
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  if (single) {
+    cp_async_wait<0>();
+    __syncthreads();          // every mover has landed
+    if (nbat > 0) store(0);
+  } else {
+    for (int b = 0; b < nbat; ++b) {
+      issue(b + kBufs - 1);   // its buffer was freed by the barrier that ended batch b - 1
+      cp_async_wait<kBufs - 1>();
+      __syncthreads();        // batch b has landed for every thread
+      store(b);
+      __syncthreads();        // batch b's buffer may be refilled
     }
-    __syncthreads();          // batch b has landed for every thread
-    store(b);
-    __syncthreads();          // batch b's half may be refilled
+    cp_async_wait<0>();
   }
   __syncthreads();
 }
