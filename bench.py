@@ -232,16 +232,25 @@ def _traffic_record(kernel_src_hash, workload, layers):
     return None
 
 
+def _hf_apply(w, compact):
+    """Hole-fill rows are moved by holefill_apply_kernel after the selection
+    when a unit's list and holes (8 B bytes) fit 56 KB of shared memory."""
+    return compact == "holefill" and 8 * w.budget <= 57344
+
+
 def _select_kernel_name(w, cap, compact):
     """The long-unit select/compact kernels tri_compress_step launches:
-    select_only_kernel then compact_only_kernel when the compaction's shared
-    memory (a 6 x 16 KB ring, 96 barrier bytes, 256 selection bytes, the kept
-    list) fits 227 KB and, for hole-fill, the ring holds the hole bookkeeping
-    (B + 16 + 4 min(B, cap - B) bytes, rounded to 128) and 16 KB of staging;
-    else select_compact_kernel."""
+    select_only_kernel, then holefill_apply_kernel (hole-fill, when _hf_apply)
+    or compact_only_kernel, when the compaction's shared memory (a 6 x 16 KB
+    ring, 96 barrier bytes, 256 selection bytes, the kept list) fits 227 KB
+    and, for hole-fill by compact_only_kernel, the ring holds the hole
+    bookkeeping (B + 16 + 4 min(B, cap - B) bytes, rounded to 128) and 16 KB of
+    staging; else select_compact_kernel."""
     B = w.budget
     bcap = -(-min(B, cap) // 32) * 32
     total = 6 * 16384 + 2 * 6 * 8 + 256 + -(-bcap * 4 // 128) * 128
+    if total <= 232448 and _hf_apply(w, compact):
+        return "select_only_kernel+holefill_apply_kernel"
     hf_ok = compact != "holefill" or -(-(B + 16 + 4 * max(min(B, cap - B), 0)) // 128) * 128 + 16384 <= 6 * 16384
     return "select_only_kernel+compact_only_kernel" if total <= 232448 and hf_ok else "select_compact_kernel"
 
@@ -356,12 +365,20 @@ def run_e2e(tk, cache, stats, params, k0, v0, idx, new_len, steps, compact):
     return t, h2d, d2h
 
 
-def _kernel_name(w, cap, compact, launches):
+def _step_kernels(w, cap, compact, fused):
+    """The kernels one tri_compress_step launches, in order (fused: the unit's
+    scores fit one CTA's shared memory; idx_out is always given here)."""
+    if fused:
+        mma = w.dtype == "bf16" and w.pairing == "half"
+        k = f"fused_mma_kernel<{w.d},{w.G}>" if mma else f"fused_kernel<{w.d},{w.G},{w.dtype}>"
+        return [k] + (["holefill_apply_kernel"] if _hf_apply(w, compact) else [])
     mma = w.dtype == "bf16" and w.pairing == "half"
-    if launches == 1:
-        return f"fused_mma_kernel<{w.d},{w.G}>" if mma else f"fused_kernel<{w.d},{w.G},{w.dtype}>"
-    return ("phase_kernel+" + ("score_keys_mma_kernel" if mma else "score_tiles_kernel") + "+"
-            + _select_kernel_name(w, cap, compact))
+    return (["phase_kernel", "score_keys_mma_kernel" if mma else "score_tiles_kernel"]
+            + _select_kernel_name(w, cap, compact).split("+"))
+
+
+def _kernel_name(w, cap, compact, fused):
+    return "+".join(_step_kernels(w, cap, compact, fused))
 
 
 class Measured:
@@ -379,9 +396,7 @@ class Measured:
         d["q_pre"] = None
         self.params = tk.Params(w.theta, d["t"], w.offsets, w.budget, pairing=w.pairing)
         self.ws = tk.workspace(self.cache, self.stats, self.params)
-        # fused kernel, or phases + scores + (select, compact | select/compact)
-        self.launches = (1 if self.ws is None else
-                         2 + len(_select_kernel_name(w, self.cache.cap, "ordered").split("+")))
+        self.fused = self.ws is None   # the unit's scores fit one CTA's shared memory
         self.k0, self.v0 = self.cache.k.clone(), self.cache.v.clone()
         self.L = self.cache.L
         self.idx = torch.empty((self.L, w.S, w.Hkv, w.budget), dtype=torch.int32, device=dev)
@@ -392,6 +407,9 @@ class Measured:
         self.cache_bytes = 2 * self.k0.numel() * self.k0.element_size()
         self.flush = (torch.empty(256 << 20, dtype=torch.uint8, device=dev)
                       if self.cache_bytes < (512 << 20) else None)
+
+    def launches(self, compact):
+        return len(_step_kernels(self.w, self.cache.cap, compact, self.fused))
 
     def restore(self):
         self.cache.k.copy_(self.k0)
@@ -477,9 +495,9 @@ def _extra(m, compact, steps, warmup, world, local, peak, note):
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                          "algorithmic_bytes_per_launch": b["alg_bytes"],
                          "algorithmic_bytes_if_all_B_moved": b["alg_bytes_all_B"],
-                         "kernel": _kernel_name(m.w, m.cache.cap, compact, m.launches)},
+                         "kernel": _kernel_name(m.w, m.cache.cap, compact, m.fused)},
             "moved_rows": b["moved_rows"], "units_compressed": b["units_compressed"],
-            "gpu_launches": m.launches * steps, "clocks": clocks}
+            "gpu_launches": m.launches(compact) * steps, "clocks": clocks}
 
 
 def decode_leg(tk, dev, windows, warmup_windows, world, local, peak, layers=None):
@@ -601,8 +619,8 @@ def run_b300(args, w):
     m = Measured(tk, w, dev)
     t_step, ms, clocks = m.time(args.compact, args.steps, args.warmup, world, local)
     b = m.bytes(args.compact)
-    head_kernel = _kernel_name(w, m.cache.cap, args.compact, m.launches)
-    head_launches, head_L = m.launches, m.L
+    head_kernel = _kernel_name(w, m.cache.cap, args.compact, m.fused)
+    head_launches, head_L = m.launches(args.compact), m.L
     l2_note = (f"cache restored from a pristine {m.cache_bytes / 1e9:.3f} GB copy before every step"
                + (" plus a 256 MB L2 flush" if m.flush is not None else " (flushes L2)") + "; untimed")
 

@@ -50,8 +50,11 @@
  *     by tri_get_device_status().  A sequence skipped for a bad block id gets
  *     new_len = N (nothing compressed); with seq_len > cap new_len is not
  *     written.  Device waits are bounded; a wait that gives
- *     up records TRI_ERR_TIMEOUT, after which the kernels of this and later calls
- *     return without work until tri_clear_device_status().
+ *     up records TRI_ERR_TIMEOUT (in the status word unless an earlier error
+ *     holds it) and sets a timeout flag, after which the kernels of this and
+ *     later calls return without work until tri_clear_device_status(); the
+ *     outputs (cache rows, idx, lengths) of the call in which a wait gave up
+ *     are then unspecified for the units it had not finished.
  *   - No C++ exception crosses this ABI.
  */
 #ifndef TRI_H
@@ -348,7 +351,8 @@ TRI_API tri_status tri_check_bounded_wait(uint32_t limit_us, cudaStream_t stream
  * receives TRI_OK or the first device-side error recorded since the last clear. */
 TRI_API tri_status tri_get_device_status(cudaStream_t stream, int32_t *out);
 
-/* Resets the device status word to TRI_OK (asynchronous on `stream`). */
+/* Resets the device status word to TRI_OK and clears the timeout flag
+ * (asynchronous on `stream`). */
 TRI_API tri_status tri_clear_device_status(cudaStream_t stream);
 
 /* Static description of a status code. */

@@ -20,6 +20,8 @@
 //                        moments in registers, one (mean, M2) per CTA.
 //   select_only_kernel   a3+a4 of the compress step for long units: kept slots.
 //   compact_only_kernel  a5 of the compress step for long units.
+//   holefill_apply_kernel a5 in the hole-fill layout after any selection that
+//                        wrote ascending kept lists: layout + independent row moves.
 //   zmax_kernel          a3 for long units (tri_score): Chan-merged moments -> agg.
 //   select_compact_kernel a3..a5 for long units whose kept list or hole-fill
 //                        bookkeeping does not fit compact_only_kernel,
@@ -114,6 +116,8 @@ struct FusedArgs {
   const int *t;
   int budget, mode, inter, capp;   // mode 0: compress, 1: score only
   int holefill;                    // compaction layout: 0 ordered, 1 hole-fill
+  int defer;                       // hole-fill: write the ascending kept list to idx_out
+                                   // and leave the rows to holefill_apply_kernel
   int mma_ok;                      // host only: try the tensor-core variant
   const tri_cache *cache;          // host only: for that variant's tensor map
   const tri_params *params;
@@ -223,13 +227,14 @@ __global__ void __launch_bounds__(kFusedThreads, (G <= 4 ? 2 : 1)) fused_kernel(
   int ntie;
   const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
   const int e0 = build_kept_chunked(keys, N, B, T, ntie, idxs, sm);
-  if (a.holefill) {   // keys are dead: their 4N bytes hold the hole-fill bookkeeping
+  if (a.holefill && !a.defer) {   // keys are dead: their 4N bytes hold the hole-fill bookkeeping
     holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), ring, kRingBytes, sm,
                   a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
     return;
   }
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
+  if (a.holefill) return;   // holefill_apply_kernel moves the rows
   // The ring was last read by generic loads (scoring); TMA writes it next.
   fence_proxy_async_smem();
   __syncthreads();
@@ -800,13 +805,14 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   int ntie;
   const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
   const int e0 = build_kept_chunked(keys, N, B, T, ntie, idxs, sm);
-  if (a.holefill) {
+  if (a.holefill && !a.defer) {
     holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), ring, kRingBytes, sm,
                   a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
     return;
   }
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
+  if (a.holefill) return;   // holefill_apply_kernel moves the rows
   // The ring was last read by ldmatrix (generic proxy); TMA writes it next.
   fence_proxy_async_smem();
   __syncthreads();
@@ -1295,10 +1301,223 @@ constexpr int kSelOnlyThreads = 256;
 constexpr int kCoThreads = 256;
 constexpr int kCoStages = 6;
 
-__global__ void __launch_bounds__(kSelOnlyThreads) select_only_kernel(const __grid_constant__ SCArgs a) {
+// Digit step of a radix select: hist[256] counts the current digit over the
+// keys still in play, and k of them are to be taken from the top.  Every
+// thread gets the digit d with S[d] >= k > S[d + 1] (S[x] = keys whose digit is
+// >= x) and the number to take among the keys with digit d.  The caller
+// synchronises between building hist and this call.  blockDim >= 256; sm: the
+// selection's shared ints ([0..1] and [8..15] here).
+__device__ __forceinline__ void radix_pick(const uint32_t *hist, int k, int *sm, uint32_t &dgt, int &k_in) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int P = 0;
+  if (tid < 256) {   // thread t scans the reversed histogram: its prefix is S[255 - t]
+    P = (int)hist[255 - tid];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, P, o);
+      if (lane >= o) P += y;
+    }
+    if (lane == 31) sm[8 + warp] = P;
+  }
+  __syncthreads();
+  if (tid < 256) {
+    int wsum = 0;
+    for (int w = 0; w < warp; ++w) wsum += sm[8 + w];
+    P += wsum;
+    int Pprev = __shfl_up_sync(0xffffffffu, P, 1);
+    if (lane == 0) Pprev = wsum;
+    if (P >= k && Pprev < k) {
+      sm[0] = 255 - tid;
+      sm[1] = k - Pprev;
+    }
+  }
+  __syncthreads();
+  dgt = (uint32_t)sm[0];
+  k_in = sm[1];
+  __syncthreads();
+}
+
+// a3 from key-major raw scores (as zmax_from_raw_km) plus the histogram of the
+// keys' top digit (the radix select's first pass).  Each thread loads U quads
+// of keys (8 16-byte loads) before using any of them.
+template <int G>
+__device__ __noinline__ void zmax_km_hist(const float *raw_u, int N, const float *mom, uint32_t *keys, uint32_t *hist) {
+  constexpr int U = G >= 8 ? 1 : 8 / G;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  float mu[G], iv[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    mu[h] = mom[h];
+    iv[h] = mom[8 + h];
+  }
+  const int n4 = (N + 3) / 4;
+  const float4 *rows = reinterpret_cast<const float4 *>(raw_u);
+  for (int q0 = tid; q0 < n4; q0 += nt * U) {
+    float4 v[U][G];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int q = q0 + k * nt;
+#pragma unroll
+      for (int h = 0; h < G; ++h) v[k][h] = q < n4 ? __ldg(rows + (long long)q * G + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int q = q0 + k * nt;
+      if (q >= n4) break;
+      float x[4 * G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        x[4 * h] = v[k][h].x;
+        x[4 * h + 1] = v[k][h].y;
+        x[4 * h + 2] = v[k][h].z;
+        x[4 * h + 3] = v[k][h].w;
+      }
+      uint32_t kk[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float z = (x[j * G] - mu[0]) * iv[0];
+#pragma unroll
+        for (int h = 1; h < G; ++h) z = fmaxf(z, (x[j * G + h] - mu[h]) * iv[h]);
+        kk[j] = score_key(z);
+        if (4 * q + j < N) atomicAdd(&hist[kk[j] >> 24], 1u);
+      }
+      reinterpret_cast<uint4 *>(keys)[q] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void zmax_km_hist_dispatch(const SCArgs &a, long long u, int N, const float *mom,
+                                                      uint32_t *keys, uint32_t *hist) {
+  const float *raw_u = a.raw + u * a.G * a.capp;
+  switch (a.G) {
+    case 1: zmax_km_hist<1>(raw_u, N, mom, keys, hist); break;
+    case 2: zmax_km_hist<2>(raw_u, N, mom, keys, hist); break;
+    case 4: zmax_km_hist<4>(raw_u, N, mom, keys, hist); break;
+    default: zmax_km_hist<8>(raw_u, N, mom, keys, hist); break;
+  }
+}
+
+// The rest of a long unit's top-K after the first digit (d1, with k to take
+// among the keys whose top digit is d1; hist holds nothing needed).  One pass
+// over the keys (each warp its contiguous segment, as the kept list's) counts
+// per warp the keys whose top digit exceeds d1, which are kept whatever their
+// other digits, and appends the keys whose top digit is d1 to cand as (key,
+// slot) pairs, histogramming their second digit.  The last three digits are
+// then resolved over the candidates alone, which also give each warp's count
+// of keys above and equal to the threshold T; a last pass writes the kept
+// slots in ascending order (those > T, then the first ntie equal to T in slot
+// order), as build_kept_gmem.  cand: room for every key of digit d1.  wc:
+// 3 nw + 1 shared ints.  Returns the first dropped slot.
+__device__ __noinline__ int select_rest_candidates(const uint32_t *keys, int n, uint32_t d1, int k, uint2 *cand,
+                                                   uint32_t *hist, int *sm, int *wc, int *idx, int K) {
+  constexpr int PF = 8;   // steps of 32 keys loaded together
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  int *cgt = wc, *gtc = wc + nw, *eqc = wc + 2 * nw, *ncand = wc + 3 * nw;
+  for (int b = tid; b < 256; b += nt) hist[b] = 0;
+  if (tid < nw) {
+    gtc[tid] = 0;
+    eqc[tid] = 0;
+  }
+  if (tid == 0) *ncand = 0;
+  __syncthreads();
+  const int seg = (((n + nw - 1) / nw) + 31) / 32 * 32;
+  const int lo = min(n, warp * seg), hi = min(n, lo + seg);
+  const unsigned lt = lanemask_lt();
+  int ngt = 0;
+  for (int base = lo; base < hi; base += 32 * PF) {
+    uint32_t u[PF];
+#pragma unroll
+    for (int e = 0; e < PF; ++e) {
+      const int i = base + 32 * e + lane;
+      u[e] = i < hi ? keys[i] : 0u;
+    }
+#pragma unroll
+    for (int e = 0; e < PF; ++e) {
+      const int i = base + 32 * e + lane;
+      const bool in = i < hi;
+      const uint32_t top = u[e] >> 24;
+      ngt += __popc(__ballot_sync(0xffffffffu, in && top > d1));
+      const unsigned m = __ballot_sync(0xffffffffu, in && top == d1);
+      if (m != 0u) {
+        int b0 = 0;
+        if (lane == 0) b0 = atomicAdd(ncand, __popc(m));
+        b0 = __shfl_sync(0xffffffffu, b0, 0);
+        if (in && top == d1) {
+          cand[b0 + __popc(m & lt)] = make_uint2(u[e], (uint32_t)i);
+          atomicAdd(&hist[(u[e] >> 16) & 255u], 1u);
+        }
+      }
+    }
+  }
+  if (lane == 0) cgt[warp] = ngt;
+  __syncthreads();   // candidates (global) and their histogram are complete
+  const int c1 = *ncand;
+  uint32_t dg;
+  radix_pick(hist, k, sm, dg, k);
+  uint32_t prefix = (d1 << 24) | (dg << 16), mask = 0xffff0000u;
+  for (int shift = 8; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += nt) hist[b] = 0;
+    __syncthreads();
+    for (int x = tid; x < c1; x += nt) {
+      const uint32_t key = cand[x].x;
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    radix_pick(hist, k, sm, dg, k);
+    prefix |= dg << shift;
+    mask |= 255u << shift;
+  }
+  const uint32_t T = prefix;
+  const int ntie = k;
+  for (int x = tid; x < c1; x += nt) {
+    const uint2 p = cand[x];
+    const int w = (int)p.y / seg;
+    if (p.x > T) atomicAdd(&gtc[w], 1);
+    else if (p.x == T) atomicAdd(&eqc[w], 1);
+  }
+  if (tid == 0) sm[56] = n;
+  __syncthreads();
+  int eq_before = 0, kept_before = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int e = eqc[w];
+    kept_before += cgt[w] + gtc[w] + max(0, min(e, ntie - eq_before));
+    eq_before += e;
+  }
+  int eq_run = eq_before, pos_run = kept_before, first_drop = n;
+  for (int base = lo; base < hi; base += 32 * PF) {
+    uint32_t u[PF];
+#pragma unroll
+    for (int e = 0; e < PF; ++e) {
+      const int i = base + 32 * e + lane;
+      u[e] = i < hi ? keys[i] : 0u;
+    }
+#pragma unroll
+    for (int e = 0; e < PF; ++e) {
+      const int i = base + 32 * e + lane;
+      const bool valid = i < hi;
+      const unsigned eqm = __ballot_sync(0xffffffffu, valid && u[e] == T);
+      const bool keep = valid && (u[e] > T || (u[e] == T && eq_run + __popc(eqm & lt) < ntie));
+      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      const unsigned dm = __ballot_sync(0xffffffffu, valid && !keep);
+      const int pos = pos_run + __popc(km & lt);
+      if (keep && pos < K) idx[pos] = i;
+      if (dm != 0u && first_drop == n) first_drop = base + 32 * e + __ffs(dm) - 1;
+      eq_run += __popc(eqm);
+      pos_run += __popc(km);
+    }
+  }
+  if (lane == 0 && first_drop < n) atomicMin(&sm[56], first_drop);
+  __syncthreads();
+  const int e0 = sm[56];
+  __syncthreads();
+  return e0;
+}
+
+__global__ void __launch_bounds__(kSelOnlyThreads, 4) select_only_kernel(const __grid_constant__ SCArgs a) {
   __shared__ uint32_t hist[256];
   __shared__ int sm[kSelInts];
   __shared__ float mom[32];
+  __shared__ int wc[3 * (kSelOnlyThreads / 32) + 1];
   const CacheView &c = a.c;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int u = blockIdx.x;
@@ -1310,19 +1529,42 @@ __global__ void __launch_bounds__(kSelOnlyThreads) select_only_kernel(const __gr
     if (tid == 0) set_status(TRI_ERR_BOUNDS);
     return;
   }
-  (void)nt;
   if (N <= B) return;            // compact_only_kernel writes its outputs
   if (!c.blocks_ok(s, N)) {      // the sequence is skipped (status recorded by compact_only_kernel)
     return;
   }
   merge_tile_moments(a.part, u, a.ntiles, a.G, N, mom, a.part_keys);
-  __syncthreads();
   uint32_t *keys = a.keys + (long long)u * a.capp;
-  zmax_dispatch<false>(a, u, N, mom, keys);
-  __syncthreads();   // the keys (global) are visible to the whole CTA
-  int ntie;
-  const uint32_t T = radix_select_gmem(keys, N, B, hist, sm, &ntie);
-  const int e0 = build_kept_gmem(keys, N, B, T, ntie, a.kept + (long long)u * B, sm);
+  int *kept = a.kept + (long long)u * B;
+  if (!a.raw_km) {   // head-major raw scores (CUDA-core score kernel)
+    __syncthreads();
+    zmax_dispatch<false>(a, u, N, mom, keys);
+    __syncthreads();   // the keys (global) are visible to the whole CTA
+    int ntie;
+    const uint32_t T = radix_select_gmem(keys, N, B, hist, sm, &ntie);
+    const int e0 = build_kept_gmem(keys, N, B, T, ntie, kept, sm);
+    if (tid == 0) a.e0s[u] = e0;
+    return;
+  }
+  for (int b = tid; b < 256; b += nt) hist[b] = 0;
+  __syncthreads();
+  zmax_km_hist_dispatch(a, u, N, mom, keys, hist);
+  __syncthreads();   // the keys (global) and the first digit's histogram are complete
+  uint32_t d1;
+  int k1;
+  radix_pick(hist, B, sm, d1, k1);
+  const int c1 = (int)hist[d1];
+  __syncthreads();
+  // the unit's raw scores are dead: their G * capp floats hold the candidates
+  uint2 *cand = reinterpret_cast<uint2 *>(const_cast<float *>(a.raw) + (long long)u * a.G * a.capp);
+  int e0;
+  if (8ll * c1 <= 4ll * a.G * a.capp) {
+    e0 = select_rest_candidates(keys, N, d1, k1, cand, hist, sm, wc, kept, B);
+  } else {
+    int ntie;
+    const uint32_t T = radix_select_gmem(keys, N, B, hist, sm, &ntie);
+    e0 = build_kept_gmem(keys, N, B, T, ntie, kept, sm);
+  }
   if (tid == 0) a.e0s[u] = e0;
 }
 
@@ -1389,6 +1631,121 @@ __global__ void __launch_bounds__(kCoThreads, 2) compact_only_kernel(const __gri
   if ((tid >> 5) < 2)
     compact_unit_tma(c, &a.maps, tid >> 5, l, s, g, idxs, e0, B, N, ring, kCoStages,
                      cbars + (tid >> 5) * kCoStages);
+}
+
+// ---------------------------------------------------------------- hole-fill moves
+// Hole-fill compaction of every unit from its ascending kept list, written by
+// the selection (the fused kernel or select_only_kernel) earlier in the step.
+// Layout: the kept slots below B stay; the r-th evicted slot below B (hole r)
+// receives the r-th kept slot at or above B (mover r).  A slot finds its
+// source without a scan: with P kept slots below B and kb of them below j
+// (binary search in the list's head), slot j is kept iff list[kb] == j, else it
+// is hole j - kb and receives list[P + j - kb].  Sources (>= B) and
+// destinations (< B) are disjoint, so the row copies are independent: after
+// the holes are ranked, each warp copies whole rows (lanes on the K pieces,
+// then the V pieces), kHfBatch movers per lane batch with every load of the
+// batch issued before its stores, and several CTAs share an SM.  Moving the
+// rows here instead of at the end of the selecting CTA keeps that CTA's tail
+// (a few row gathers at full latency) off the streaming kernel.
+constexpr int kHfThreads = 256;
+constexpr int kHfBatch = 4;
+
+struct HfArgs {
+  CacheView c;
+  int budget;
+  const int *kept;   // [units][B] ascending kept slots (may alias idx_out)
+  int *idx_out;      // [units][B] or null: the layout (original slot now at j)
+  int *new_len;      // [S] or null
+  int outputs;       // 1: also the lengths and the identity idx of units with N <= B
+};
+
+// Dynamic shared memory of holefill_apply_kernel: the list, then the holes.
+__host__ __device__ __forceinline__ int hf_apply_smem(int B) { return 8 * B; }
+
+__global__ void __launch_bounds__(kHfThreads, 4) holefill_apply_kernel(const __grid_constant__ HfArgs a) {
+  extern __shared__ __align__(16) int hsm[];
+  const CacheView &c = a.c;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  const int u = blockIdx.x;
+  const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
+  if (timed_out()) return;   // a selection may have stopped before writing its list
+  const int N = c.seq_len[s];
+  const int B = a.budget;
+  if (N < 0 || N > c.cap) {
+    if (a.outputs && tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  const bool len_writer = a.outputs && tid == 0 && a.new_len != nullptr && l == 0 && g == 0;
+  if (N <= B) {
+    if (a.outputs) {
+      if (len_writer) a.new_len[s] = N;
+      if (a.idx_out != nullptr)
+        for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = j < N ? j : -1;
+    }
+    return;
+  }
+  if (!c.blocks_ok(s, N)) {   // the sequence is skipped: its length stays N
+    if (a.outputs) {
+      if (tid == 0) set_status(TRI_ERR_BOUNDS);
+      if (len_writer) a.new_len[s] = N;
+    }
+    return;
+  }
+  int *list = hsm, *holes = hsm + B;
+  const int *src = a.kept + (long long)u * B;
+  for (int j = tid; j < B; j += nt) list[j] = src[j];
+  __syncthreads();
+  int bad = 0;
+  for (int j = tid; j < B; j += nt) bad |= (list[j] < 0) | (list[j] >= N) | (j > 0 && list[j] <= list[j - 1]);
+  if (__syncthreads_or(bad)) {   // every read of the list in global memory is done
+    if (tid == 0) set_status(TRI_ERR_INVALID);
+    if (len_writer) a.new_len[s] = N;
+    return;
+  }
+  if (len_writer) a.new_len[s] = B;
+  int lo = 0, hi = B;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (list[mid] < B) lo = mid + 1; else hi = mid;
+  }
+  const int P = lo, M = B - P;
+  for (int j = tid; j < B; j += nt) {
+    int kl = 0, kh = P;
+    while (kl < kh) {
+      const int mid = (kl + kh) >> 1;
+      if (list[mid] < j) kl = mid + 1; else kh = mid;
+    }
+    const bool stays = kl < P && list[kl] == j;
+    if (!stays) holes[j - kl] = j;
+    if (a.idx_out != nullptr) a.idx_out[(long long)u * B + j] = stays ? j : list[P + j - kl];
+  }
+  __syncthreads();
+  // mover r: row list[P + r] -> row holes[r], K then V; 16-byte pieces, lane
+  // q (and q + 32) of the warp on piece q of the K and V rows together
+  const int ppr = c.rb >> 4, pp = 2 * ppr;
+  for (int r0 = warp * kHfBatch; r0 < M; r0 += nw * kHfBatch) {
+    long long so[kHfBatch], dof[kHfBatch];
+#pragma unroll
+    for (int b = 0; b < kHfBatch; ++b) {
+      const int r = r0 + b;
+      so[b] = r < M ? c.row_off(l, s, g, list[P + r]) : -1;
+      dof[b] = r < M ? c.row_off(l, s, g, holes[r]) : -1;
+      if (dof[b] < 0) so[b] = -1;
+    }
+    for (int e = 0; 32 * e < pp; ++e) {   // one or two rounds of 16-byte pieces
+      const int q = lane + 32 * e;
+      const bool kq = q < ppr;
+      const int col = (kq ? q : q - ppr) * 16;
+      const bool in = q < pp;
+      uint4 v[kHfBatch];
+#pragma unroll
+      for (int b = 0; b < kHfBatch; ++b)
+        if (in && so[b] >= 0) v[b] = *reinterpret_cast<const uint4 *>((kq ? c.k : c.v) + so[b] + col);
+#pragma unroll
+      for (int b = 0; b < kHfBatch; ++b)
+        if (in && so[b] >= 0) *reinterpret_cast<uint4 *>((kq ? c.k : c.v) + dof[b] + col) = v[b];
+    }
+  }
 }
 
 // ================================================================ host side
@@ -1640,6 +1997,28 @@ static tri_status set_smem(K kernel, int bytes) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
     return TRI_ERR_CUDA;
   return TRI_OK;
+}
+
+// Hole-fill rows are moved after the selection, by holefill_apply_kernel, when
+// a unit's list and holes (8 B bytes) fit 56 KB of shared memory (four CTAs
+// per SM at least); else the selecting kernel moves them itself.
+constexpr int kHfMaxSmem = 57344;
+static bool hf_apply_ok(int B) { return hf_apply_smem(B) <= kHfMaxSmem; }
+
+static tri_status run_holefill_apply(const CacheView &view, int B, const int *kept, int32_t *idx_out,
+                                     int32_t *new_len, int outputs, int64_t units, cudaStream_t st) {
+  HfArgs h;
+  std::memset(&h, 0, sizeof(h));
+  h.c = view;
+  h.budget = B;
+  h.kept = kept;
+  h.idx_out = idx_out;
+  h.new_len = new_len;
+  h.outputs = outputs;
+  const int bytes = hf_apply_smem(B);
+  if (set_smem(holefill_apply_kernel, bytes) != TRI_OK) return TRI_ERR_CUDA;
+  holefill_apply_kernel<<<(unsigned)units, kHfThreads, bytes, st>>>(h);
+  return launch_result();
 }
 
 template <int D, int G, bool BF16>
@@ -2040,9 +2419,13 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
     FusedArgs a = fused_args(cache, stats, params);
     a.mode = 0;
     a.holefill = mode == TRI_COMPACT_HOLEFILL;
+    // hole-fill: the fused kernel selects and writes the kept list to idx_out,
+    // holefill_apply_kernel turns it into the layout and moves the rows
+    a.defer = a.holefill && idx_out != nullptr && hf_apply_ok(params->budget);
     a.idx_out = idx_out;
     a.new_len = new_len;
-    return TRI_DISPATCH(run_fused, cache->d, G, bf16, a, units, stream);
+    if ((e = TRI_DISPATCH(run_fused, cache->d, G, bf16, a, units, stream)) != TRI_OK || !a.defer) return e;
+    return run_holefill_apply(a.c, params->budget, idx_out, idx_out, new_len, 0, units, stream);
   }
   const SplitWs w = split_ws(cache, G, params->budget);
   if (ws == nullptr || ws_bytes < w.total || !aligned16(ws)) return TRI_ERR_WORKSPACE;
@@ -2089,9 +2472,12 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   // stays for staging the moved rows
   const bool hf_fits = !sa.holefill || align_up(params->budget + 16 + 4 * (int)std::max<int64_t>(movers, 0), 128) +
                                                16384 <= kCoStages * kStageBytes;
-  const bool split = co.total <= kMaxSmem && hf_fits;
+  // hole-fill with holefill_apply_kernel after the selection: the kept list
+  // goes to idx_out (rewritten there as the layout) or the workspace
+  const bool apply = sa.holefill && hf_apply_ok(params->budget);
+  const bool split = co.total <= kMaxSmem && (apply || hf_fits);
   if (split) {
-    sa.kept = (!sa.holefill && idx_out != nullptr) ? idx_out : reinterpret_cast<int *>(wsb + w.kept_off);
+    sa.kept = ((!sa.holefill || apply) && idx_out != nullptr) ? idx_out : reinterpret_cast<int *>(wsb + w.kept_off);
     sa.e0s = reinterpret_cast<int *>(wsb + w.e0_off);
   }
   if ((e = run_phases(cache, ta, stream)) != TRI_OK) return e;
@@ -2099,6 +2485,7 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   if (!split) return run_select_compact(sa, units, stream);
   select_only_kernel<<<(unsigned)units, kSelOnlyThreads, 0, stream>>>(sa);
   if ((e = launch_result()) != TRI_OK) return e;
+  if (apply) return run_holefill_apply(sa.c, params->budget, sa.kept, idx_out, new_len, 1, units, stream);
   if (set_smem(compact_only_kernel, co.total) != TRI_OK) return TRI_ERR_CUDA;
   compact_only_kernel<<<(unsigned)units, kCoThreads, co.total, stream>>>(sa);
   return launch_result();
@@ -2327,7 +2714,9 @@ tri_status tri_get_device_status(cudaStream_t stream, int32_t *out) {
 tri_status tri_clear_device_status(cudaStream_t stream) {
   static const int zero = 0;
   if (cudaMemcpyToSymbolAsync(g_tri_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream) !=
-      cudaSuccess)
+          cudaSuccess ||
+      cudaMemcpyToSymbolAsync(g_tri_timeout, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream) !=
+          cudaSuccess)
     return TRI_ERR_CUDA;
   return TRI_OK;
 }

@@ -35,14 +35,19 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // bounded device w
 
 // First device-side error since the last clear (0 = TRI_OK).
 __device__ int g_tri_status = 0;
+// Nonzero once some wait has given up since the last clear, whichever error
+// the status word holds (an earlier error keeps its place there).
+__device__ int g_tri_timeout = 0;
 
 __device__ __forceinline__ void set_status(int code) { atomicCAS(&g_tri_status, 0, code); }
 
-// True once some wait has given up (TRI_ERR_TIMEOUT recorded and not yet
-// cleared): kernels that wait on copies then leave at once instead of waiting
-// out their own limits one CTA after another.
+// True once some wait has given up (and the flags are not yet cleared):
+// kernels that wait on copies then leave at once instead of waiting out their
+// own limits one CTA after another, and kernels that consume a list an earlier
+// kernel of the step wrote do not trust lists that kernel may have left
+// unwritten.
 __device__ __forceinline__ bool timed_out() {
-  return *reinterpret_cast<volatile int *>(&g_tri_status) == TRI_ERR_TIMEOUT;
+  return *reinterpret_cast<volatile int *>(&g_tri_timeout) != 0;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -91,6 +96,7 @@ __device__ __noinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, uint6
       if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > limit_ns) {
       set_status(TRI_ERR_TIMEOUT);
+      atomicExch(&g_tri_timeout, 1);
       return false;
     }
   }

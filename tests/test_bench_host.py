@@ -2,7 +2,8 @@
 
 The bench line names the kernels a step launches; for long units that name
 follows the library's own rule for choosing select_only_kernel +
-compact_only_kernel (the compaction's shared-memory layout and ring size).  These tests restate that rule from the constants in the
+compact_only_kernel or + holefill_apply_kernel (the compaction's shared-memory
+layout and ring size, the hole-fill kernel's shared-memory cap).  These tests restate that rule from the constants in the
 CUDA sources and check bench.py's copy of it, so the two cannot drift apart.
 """
 import os
@@ -32,6 +33,8 @@ def _rule(B, cap, compact):
     up = lambda x, a: -(-x // a) * a
     bcap = up(min(B, cap), 32)
     total = stages * stage + 2 * stages * 8 + sel_ints * 4 + up(bcap * 4, 128)
+    if total <= max_smem and compact == "holefill" and 8 * B <= _const("kHfMaxSmem"):
+        return "select_only_kernel+holefill_apply_kernel"
     hf_ok = compact != "holefill" or up(B + 16 + 4 * max(min(B, cap - B), 0), 128) + 16384 <= stages * stage
     return "select_only_kernel+compact_only_kernel" if total <= max_smem and hf_ok else "select_compact_kernel"
 
@@ -51,3 +54,10 @@ def test_moved_rows_counts_only_compressed_units():
     seq_len = torch.tensor([4, 9], dtype=torch.int32)
     # sequence 0 has N <= B (untouched); sequence 1 keeps slot 0 in place and moves 3 rows
     assert bench._moved_rows(idx, seq_len, B) == 3
+
+
+@pytest.mark.parametrize("compact", ["ordered", "holefill"])
+def test_fused_step_kernels(compact):
+    w = WORKLOADS["qwen3_8b_36l_b16_n2176"]
+    k = bench._step_kernels(w, 2176, compact, fused=True)
+    assert k == ["fused_mma_kernel<128,4>"] + (["holefill_apply_kernel"] if compact == "holefill" else [])

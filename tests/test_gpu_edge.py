@@ -72,13 +72,15 @@ def test_budget_boundaries_and_t_offset():
     C.run_and_check(w2, data, units, DEV)
 
 
-@pytest.mark.parametrize("n_keys", [800, 20000])
-def test_all_zero_keys_tie_everywhere(n_keys):
+@pytest.mark.parametrize("n_keys,Hq", [(800, 4), (20000, 4), (20000, 2)])
+def test_all_zero_keys_tie_everywhere(n_keys, Hq):
     """A unit whose keys are all zero (a cleared or padded region): every score
     is exactly 0 on both sides, the z-score of each head is 0/0 := 0, all keys
     tie, the lowest B slots are kept and nothing moves (fused path at N = 800,
-    split path at N = 20000)."""
-    w = W(f"edge_ties_{n_keys}", Hq=4, S=1, Hkv=2, budget=300, n_keys=n_keys)
+    split path at N = 20000).  On the split path every key is a candidate after
+    the first digit: at G = 2 the candidate pairs just fit the unit's dead raw
+    scores, at G = 1 they do not and the selection takes its full-pass route."""
+    w = W(f"edge_ties_{n_keys}_g{Hq // 2}", Hq=Hq, S=1, Hkv=2, budget=300, n_keys=n_keys)
     data = generate(w, device=DEV)
     data["k"][0, 0, 1].zero_()          # KV head 1
     # the zero unit must keep exactly slots 0..B-1: no difference, even in the tie band
@@ -92,6 +94,9 @@ HOLEFILL_CASES = [
     W("hf_long_mma_g4", Hq=8, n_range=(9000, 13000), budget=1024),
     W("hf_long_mma_g8_paged", Hq=16, n_range=(12000, 16000), budget=1024, paged=True),
     W("hf_long_cuda_f32", Hq=4, d=64, dtype="f32", n_range=(30000, 40000), budget=2048, S=2),
+    # B = 8192: the list and holes (64 KB) exceed holefill_apply_kernel's cap, so
+    # compact_only_kernel moves the rows itself
+    W("hf_long_mma_b8192_in_compaction", Hq=8, n_range=(18000, 26000), budget=8192, S=2),
 ]
 
 
@@ -100,3 +105,34 @@ def test_holefill_every_unit(w):
     data = generate(w, device=DEV)
     units = [(0, s, g) for s in range(w.S) for g in range(w.Hkv)]
     C.run_and_check_holefill(w, data, units, DEV)
+
+
+DEFER_CASES = [
+    W("hf_defer_fused_g4", Hq=8, n_range=(600, 1900), budget=700),
+    W("hf_defer_fused_g8", Hq=16, n_range=(1000, 3000), budget=1024),
+    W("hf_defer_fused_paged16_g4", Hq=8, n_range=(700, 2500), paged=True),
+    W("hf_defer_fused_f32_inter_g2", Hq=4, d=64, dtype="f32", pairing="interleaved", n_range=(500, 1500)),
+]
+
+
+@pytest.mark.parametrize("w", DEFER_CASES, ids=[w.name for w in DEFER_CASES])
+def test_holefill_moves_without_idx_out_match_the_apply_kernel(w):
+    """With idx_out the fused kernel leaves the hole-fill moves to
+    holefill_apply_kernel; without it the fused kernel moves the rows itself.
+    Both give the same cache, bit for bit, and the same lengths."""
+    import kv_cache_compression_06_b300 as tk
+    data = generate(w, device=DEV)
+    out = []
+    for with_idx in (True, False):
+        cache, stats, params = C.setup(w, data, DEV)
+        cache = tk.KVCache(cache.k.clone(), cache.v.clone(), cache.seq_len, Hkv=w.Hkv,
+                           block_table=cache.block_table, block=w.block)
+        L = cache.k.shape[0]
+        idx = torch.full((L, w.S, w.Hkv, w.budget), -7, dtype=torch.int32, device=DEV) if with_idx else None
+        new_len = torch.full((w.S,), -7, dtype=torch.int32, device=DEV)
+        tk.tri_compress_step(cache, stats, params, idx_out=idx, new_len=new_len, compact="holefill")
+        torch.cuda.synchronize()
+        assert tk.tri_get_device_status() == 0
+        out.append((cache.k, cache.v, new_len))
+    assert torch.equal(out[0][2], out[1][2])
+    assert torch.equal(out[0][0], out[1][0]) and torch.equal(out[0][1], out[1][1])
