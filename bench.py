@@ -373,8 +373,10 @@ def _step_kernels(w, cap, compact, fused):
         k = f"fused_mma_kernel<{w.d},{w.G}>" if mma else f"fused_kernel<{w.d},{w.G},{w.dtype}>"
         return [k] + (["holefill_apply_kernel"] if _hf_apply(w, compact) else [])
     mma = w.dtype == "bf16" and w.pairing == "half"
-    return (["phase_kernel", "score_keys_mma_kernel" if mma else "score_tiles_kernel"]
-            + _select_kernel_name(w, cap, compact).split("+"))
+    # paged d = 128 caches whose block holds 128 head-rows: every KV head of a block per copy
+    heads = mma and w.paged and w.d == 128 and w.Hkv * w.block == 128 and w.block % 16 == 0
+    score = "score_heads_mma_kernel" if heads else ("score_keys_mma_kernel" if mma else "score_tiles_kernel")
+    return ["phase_kernel", score] + _select_kernel_name(w, cap, compact).split("+")
 
 
 def _kernel_name(w, cap, compact, fused):

@@ -272,6 +272,7 @@ struct TileArgs {
   int Hq;
   const int *t;
   int budget, skip_small, inter, ntiles, mma_ok;
+  int hg;            // ks boxes every KV head of a block: score_heads_mma_kernel
   long long raw_stride;
   const float2 *phase;   // [S][F] step phases (phase_kernel); raw_stride: floats between the raw rows of two heads (cap, or capp in the workspace)
   float *raw;      // [(u*G + h)*raw_stride + i]
@@ -1032,6 +1033,177 @@ __global__ void __launch_bounds__(kThreads, 2) score_keys_mma_kernel(const __gri
   }
 }
 
+// ---------------------------------------------------------------- long units, paged: every KV head of a block
+// score_keys_mma_kernel for paged bf16 caches (d = 128, rotate-half bands)
+// whose block holds 128 head-rows (Hkv x block = 128: 8 heads of 16 rows, or 4
+// of 32): a CTA scores all KV heads of one (layer, sequence) over kHgKeys
+// keys, and each stage is one whole block, 32 KB contiguous in HBM, brought in
+// by one tensor copy (box: 64 elements x block rows x 2 halves x Hkv heads),
+// instead of one 4 KB copy per block and head with the rows 2 KB apart.  In
+// shared memory the stage is [head][half][block rows][128 B], each head's part
+// laid out as a one-block stage of the per-head kernel.  16 consumer warps:
+// warp w takes tile w % 8 of the stages with parity w / 8 (a stage holds 8
+// 16-row tiles, Hkv x block / 16), i.e. the rows 16 (tile % TPH) .. of head
+// tile / TPH (TPH = block / 16 tiles per head).  Raw scores and the lanes'
+// moments as score_keys_mma_kernel, one (mean, M2) entry per CTA and head.
+// One CTA per SM (17 warps) with a 6 x 32 KB ring.  The consumers build the
+// fp32 weights of all the CTA's heads in ring slots 4 and 5 and take their
+// fragments (G = 8: lo fragments to a region of their own) while the producer
+// fills slots 0 to 3; it issues slot 4 only once every consumer has passed
+// named barrier 2.  The stage count is even so that every ring slot is only
+// ever read by the warps of one parity: a warp then waits on each phase of its
+// slots' full barriers in turn, and a parity wait cannot match a phase two
+// back (a slot shared by both parities would let a warp that ran a cycle
+// ahead see the previous use's completed phase as its own).
+constexpr int kHgKeys = 2048;       // keys per CTA and head (one part entry)
+constexpr int kHgStages = 6;
+constexpr int kHgEarly = 4;         // stages issued before the weights are taken
+static_assert(kHgStages % 2 == 0, "ring slots must belong to one consumer parity");
+constexpr int kHgStageBytes = 32768;
+constexpr int kHgConsumers = 16;
+constexpr int kHgThreads = (kHgConsumers + 1) * 32;
+
+struct HgLayout {
+  int bars, wts, lo, red, total;
+  __host__ __device__ HgLayout(int G, int F, int Hkv) {
+    int o = kHgStages * kHgStageBytes;
+    wts = kHgEarly * kHgStageBytes;                    // [Hkv][G][3][F] fp32, in ring slots 4 and 5
+    bars = o;  o += 256;                               // full[6], empty[6], fail, issued
+    lo = o;    o += G == 8 ? Hkv * (3 * F / 16) * 32 * 8 : 0;   // G = 8: [Hkv][12 k-steps][32 lanes] lo fragments
+    red = o;   o += kHgConsumers * 4 * 5 * 4;
+    total = o;
+  }
+};
+
+template <int G>
+__global__ void __launch_bounds__(kHgThreads, 1) score_heads_mma_kernel(const __grid_constant__ TileArgs a) {
+  constexpr int D = 128, F = 64, NC = kHgConsumers * 32;
+  extern __shared__ __align__(1024) char smem[];
+  const CacheView &c = a.c;
+  const HgLayout lay(G, F, c.Hkv);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
+  uint64_t *empty = full + kHgStages;
+  volatile int *fail = reinterpret_cast<volatile int *>(empty + kHgStages);
+  volatile int *issued = fail + 1;
+  float *wts = reinterpret_cast<float *>(smem + lay.wts);
+  float *lo = reinterpret_cast<float *>(smem + lay.lo);
+  float *red = reinterpret_cast<float *>(smem + lay.red);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ls = blockIdx.y;
+  const int s = ls % c.S, l = ls / c.S;
+  if (timed_out()) return;
+  const int N = c.seq_len[s];
+  if (N < 0 || N > c.cap) {
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  if (a.skip_small && N <= a.budget) return;
+  const int i0 = blockIdx.x * kHgKeys;
+  if (i0 >= N) return;
+  const int n = min(kHgKeys, N - i0);
+  if (!c.blocks_ok(s, n, i0)) {
+    if (tid == 0) set_status(TRI_ERR_BOUNDS);
+    return;
+  }
+  const int blk = c.block, TPH = blk / 16;
+  const int nst = (n + blk - 1) / blk;
+  if (tid == 0) {
+    for (int st = 0; st < kHgStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 8);   // the 8 consumer warps of the stage's parity
+    }
+    *fail = 0;
+    *issued = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == kHgConsumers) {   // producer: one copy per block, all heads
+    int t = 0;
+    bool taken = false;   // the consumers hold their weights: slots kHgEarly.. are free
+    for (; t < nst; ++t) {
+      if (t == kHgEarly) {
+        named_sync(2, kHgThreads);
+        taken = true;
+      }
+      const int st = t % kHgStages;
+      if (*fail || (t >= kHgStages && !mbar_wait(&empty[st], (uint32_t)(((t / kHgStages) - 1) & 1)))) {
+        *fail = 1;
+        break;
+      }
+      if (lane == 0) {
+        const int b = c.bt[(long long)s * c.max_blocks + i0 / blk + t];
+        mbar_arrive_expect_tx(&full[st], (uint32_t)(c.Hkv * blk * 256));
+        tma_load_5d(smem + st * kHgStageBytes, &a.ks, 0, 0, 0, 0, (int)((long long)l * c.nblocks + b), &full[st]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) *issued = t;
+    if (!taken) named_sync(2, kHgThreads);
+  } else {
+    for (int hh = 0; hh < c.Hkv; ++hh)
+      build_weights<G, F>(wts + hh * G * 3 * F, a.center, a.R, a.mag, a.Hq, l, hh, a.t[s], a.sc,
+                          a.phase + (long long)s * F, NC);
+    named_sync(1, NC);
+    const int tile = warp & 7, par = warp >> 3;
+    const int h = tile / TPH, sub = tile - h * TPH;
+    MmaWeights<D, G> w;
+    load_mma_weights<D, G>(w, wts + h * G * 3 * F, NC, par == 0 && sub == 0, lo + h * (3 * F / 16) * 32 * 2);
+    fence_proxy_async_smem();    // slots 4 and 5 were written by plain stores; tensor copies refill them
+    named_sync(2, kHgThreads);   // the weights there are dead: the producer may refill them
+    const uint32_t ring = smem_u32(smem);
+    const long long u = (long long)ls * c.Hkv + h;
+    float *raw_c = a.raw + ((long long)u * a.raw_stride + i0) * G;   // this CTA's first key of head h
+    const int r = lane >> 2, n0 = 2 * (lane & 3);
+    const bool holds = G == 8 || n0 < G;
+    LaneMoments lm;
+    for (int t = par; t < nst; t += 2) {
+      const int st = t % kHgStages;
+      if (!*fail && !mbar_wait(&full[st], (uint32_t)((t / kHgStages) & 1))) *fail = 1;
+      float o[4];
+      score_tile_mma_frag<D, G, 64>(ring + st * kHgStageBytes + h * (2 * blk * 128), 16 * sub, w, blk, o);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);   // the stage's rows are in registers
+      if (*fail) continue;
+      const int kb = t * blk + 16 * sub;        // CTA-local key of this tile's row 0
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int key = kb + r + 8 * hh;
+        if (holds && key < n) {
+          const float x0 = o[2 * hh], x1 = o[2 * hh + 1];
+          if constexpr (G == 1)
+            raw_c[key] = x0;
+          else
+            *reinterpret_cast<float2 *>(raw_c + (long long)key * G + n0) = make_float2(x0, x1);
+          lm.add(x0, x1);
+        }
+      }
+    }
+    lm.to_shared(red, warp);
+  }
+  __syncthreads();
+  if (*fail) {
+    if (tid == 0) {
+      const int iss = *issued;
+      for (int st = 0; st < kHgStages && st < iss; ++st) {
+        const int last = st + ((iss - 1 - st) / kHgStages) * kHgStages;
+        mbar_wait(&full[st], (uint32_t)((last / kHgStages) & 1));
+      }
+    }
+    return;
+  }
+  if (tid < c.Hkv * G) {   // (KV head, query head of its group): merge the warps of that KV head
+    const int h = tid / G, qh = tid - h * G, cls = qh / 2, j = qh & 1;
+    float nn = 0.f, mm = 0.f, qq = 0.f;
+    for (int wp = 0; wp < kHgConsumers; ++wp) {
+      if ((wp & 7) / TPH != h) continue;
+      const float *rw = red + (wp * 4 + cls) * 5;
+      chan_merge(nn, mm, qq, rw[0], rw[1 + j], rw[3 + j]);
+    }
+    const long long u = (long long)ls * c.Hkv + h;
+    a.part[((long long)u * a.ntiles + blockIdx.x) * G + qh] = make_float2(mm, qq);
+  }
+}
+
 struct ZArgs {
   int S, Hkv, G, ntiles;
   long long cap, raw_stride;
@@ -1410,7 +1582,7 @@ __device__ __forceinline__ void zmax_km_hist_dispatch(const SCArgs &a, long long
 // 3 nw + 1 shared ints.  Returns the first dropped slot.
 __device__ __noinline__ int select_rest_candidates(const uint32_t *keys, int n, uint32_t d1, int k, uint2 *cand,
                                                    uint32_t *hist, int *sm, int *wc, int *idx, int K) {
-  constexpr int PF = 8;   // steps of 32 keys loaded together
+  constexpr int PF = 16;  // steps of 32 keys loaded together (the passes are bound by L2 latency)
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
   int *cgt = wc, *gtc = wc + nw, *eqc = wc + 2 * nw, *ncand = wc + 3 * nw;
   for (int b = tid; b < 256; b += nt) hist[b] = 0;
@@ -1513,8 +1685,263 @@ __device__ __noinline__ int select_rest_candidates(const uint32_t *keys, int n, 
   return e0;
 }
 
+// ---- long-unit selection in one pass over the raw scores
+// A sample of kSampleKeys keys (every (N / kSampleKeys)-th slot) locates the
+// B-th largest key to a range of 12-bit digits [d_lo, d_hi] (the sample ranks
+// p ns -/+ (4 sqrt(ns p (1 - p)) + 4), p = B / N).  One pass over the raw
+// scores then turns every key into its z/max key and sorts it three ways
+// without storing it: digit > d_hi sets the key's bit in a kept bitmask in
+// shared memory (8 lanes assemble a 32-slot word from their quads' nibbles);
+// d_lo <= digit <= d_hi appends (key, slot) to a candidate list in the unit's
+// (dead) key region; below d_lo nothing.  If the count above d_hi is below B
+// and the candidates reach B, the threshold T is the (B - above)-th largest
+// candidate (a 4 x 8-bit radix select over the candidates only); candidates
+// above T set their bits, those equal to T mark a second bitmask, of which the
+// first ntie in slot order join the kept set; a scan over the words writes
+// the kept slots in ascending order.  Same result as the full passes (kept =
+// keys > T, then the first ntie keys equal to T in slot order); the raw scores
+// are read once and no key array is written.  Returns false, with nothing
+// written, when the sample's range missed T or the candidates overflow: the
+// caller then runs the full passes.
+constexpr int kSampleKeys = 1024;
+constexpr int kBmMaxKeys = 65536;   // bitmask words in shared memory: 2 x 8 KB
+
+template <int G>
+__device__ __forceinline__ uint32_t zkey_of(const float *raw_u, int i, const float *mu, const float *iv) {
+  const float *x = raw_u + (long long)i * G;
+  float z = (x[0] - mu[0]) * iv[0];
+#pragma unroll
+  for (int h = 1; h < G; ++h) z = fmaxf(z, (x[h] - mu[h]) * iv[h]);
+  return score_key(z);
+}
+
+// Digits of the (r0 + 1)-th and (r1 + 1)-th largest keys counted in hist[4096]
+// (12-bit digits): thread t (blockDim 256) owns bins [4080 - 16 t, 4096 - 16 t).
+__device__ __forceinline__ void pick12(const uint32_t *hist, int r0, int r1, int *sm, uint32_t &d0, uint32_t &d1) {
+  const int tid = threadIdx.x;
+  const int top = 4095 - 16 * tid;
+  int cnt = 0;
+#pragma unroll 4
+  for (int b = 0; b < 16; ++b) cnt += (int)hist[top - b];
+  int tot;
+  const int before = block_excl_scan(cnt, sm, &tot);
+  if (tid == 0) {
+    sm[40] = 0;
+    sm[41] = 0;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int r = q == 0 ? r0 : r1;
+    if (r >= before && r < before + cnt) {
+      int run = before;
+      for (int b = 0; b < 16; ++b) {
+        run += (int)hist[top - b];
+        if (run > r) {
+          sm[40 + q] = top - b;
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  d0 = (uint32_t)sm[40];
+  d1 = (uint32_t)sm[41];
+  __syncthreads();
+}
+
+template <int G>
+__device__ __noinline__ bool select_one_pass(const float *raw_u, int N, int B, const float *mom, uint32_t *hist,
+                                             uint32_t *bm, uint32_t *eqm, int *sm, uint2 *cand, int cand_cap,
+                                             int *idx, int *e0_out) {
+  constexpr int U = G >= 8 ? 1 : 8 / G;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
+  float mu[G], iv[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    mu[h] = mom[h];
+    iv[h] = mom[8 + h];
+  }
+  const int W = (N + 31) / 32, n4 = (N + 3) / 4;
+  for (int b = tid; b < 4096; b += nt) hist[b] = 0;
+  for (int w = tid; w < W; w += nt) {
+    bm[w] = 0;
+    eqm[w] = 0;
+  }
+  if (tid == 0) {
+    sm[48] = 0;   // keys above d_hi
+    sm[49] = 0;   // candidates
+    sm[50] = 0;   // candidate overflow
+  }
+  __syncthreads();
+  // the sample
+  const int ns = min(kSampleKeys, N);
+  for (int j = tid; j < ns; j += nt) {
+    const int i = (int)(((long long)j * N) / ns);
+    atomicAdd(&hist[zkey_of<G>(raw_u, i, mu, iv) >> 20], 1u);
+  }
+  __syncthreads();
+  const float p = (float)B / (float)N;
+  const float m = 4.0f * sqrtf((float)ns * p * (1.0f - p)) + 4.0f;
+  const int r_hi = max(0, (int)floorf(p * ns - m)), r_lo = min(ns - 1, (int)ceilf(p * ns + m));
+  uint32_t d_hi, d_lo;
+  pick12(hist, r_hi, r_lo, sm, d_hi, d_lo);
+  // the pass: warp-uniform loop over rounds of U quads per lane
+  const float4 *rows = reinterpret_cast<const float4 *>(raw_u);
+  for (int q0 = tid - lane; q0 < n4; q0 += nt * U) {
+    float4 v[U][G];   // quads q = q0 + lane + k nt: the 4 G key-major scores of keys 4q .. 4q + 3
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int q = q0 + lane + k * nt;
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        v[k][h] = q < n4 ? __ldg(rows + (long long)q * G + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int q = q0 + lane + k * nt;
+      float x[4 * G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        x[4 * h] = v[k][h].x;
+        x[4 * h + 1] = v[k][h].y;
+        x[4 * h + 2] = v[k][h].z;
+        x[4 * h + 3] = v[k][h].w;
+      }
+      uint32_t nib = 0, ck[4];
+      int cc = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float z = (x[j * G] - mu[0]) * iv[0];
+#pragma unroll
+        for (int h = 1; h < G; ++h) z = fmaxf(z, (x[j * G + h] - mu[h]) * iv[h]);
+        const uint32_t key = score_key(z), dg = key >> 20;
+        const bool in = q < n4 && 4 * q + j < N;
+        ck[j] = key;
+        if (in && dg > d_hi) nib |= 1u << j;
+        else if (in && dg >= d_lo) cc |= 1 << j;   // candidate mask
+      }
+      // the word of slots 32 (q >> 3) .. : 8 consecutive lanes' nibbles
+      uint32_t word = nib << (4 * (lane & 7));
+      word |= __shfl_xor_sync(0xffffffffu, word, 1);
+      word |= __shfl_xor_sync(0xffffffffu, word, 2);
+      word |= __shfl_xor_sync(0xffffffffu, word, 4);
+      if ((lane & 7) == 0 && q < n4) bm[q >> 3] = word;
+      const int na = __reduce_add_sync(0xffffffffu, __popc(nib));
+      // candidates: one atomic per warp, positions by an inclusive scan of the lanes' counts
+      const int nc = __popc((unsigned)cc);
+      int incl = nc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int base = 0;
+      if (lane == 31) {
+        if (na) atomicAdd(&sm[48], na);
+        base = incl > 0 ? atomicAdd(&sm[49], incl) : 0;
+      }
+      base = __shfl_sync(0xffffffffu, base, 31) + incl - nc;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (cc & (1 << j)) {
+          if (base < cand_cap) cand[base] = make_uint2(ck[j], (uint32_t)(4 * q + j));
+          else sm[50] = 1;
+          ++base;
+        }
+    }
+  }
+  __syncthreads();
+  const int above = sm[48], c = sm[49];
+  const int k_in = B - above;
+  if (sm[50] != 0 || k_in < 1 || k_in > c) {
+    __syncthreads();
+    return false;
+  }
+  // T: the k_in-th largest candidate
+  uint32_t prefix = 0, mask = 0;
+  int k = k_in;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += nt) hist[b] = 0;
+    __syncthreads();
+    for (int x = tid; x < c; x += nt) {
+      const uint32_t key = cand[x].x;
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    uint32_t dg;
+    radix_pick(hist, k, sm, dg, k);
+    prefix |= dg << shift;
+    mask |= 255u << shift;
+  }
+  const uint32_t T = prefix;
+  const int ntie = k;
+  for (int x = tid; x < c; x += nt) {
+    const uint2 pr = cand[x];
+    if (pr.x > T) atomicOr(&bm[pr.y >> 5], 1u << (pr.y & 31));
+    else if (pr.x == T) atomicOr(&eqm[pr.y >> 5], 1u << (pr.y & 31));
+  }
+  if (tid == 0) sm[56] = N;
+  __syncthreads();
+  // the first ntie keys equal to T in slot order, then the kept slots in order;
+  // thread t owns words [t wpt, (t + 1) wpt)
+  const int wpt = (W + nt - 1) / nt, w0 = min(W, tid * wpt), w1 = min(W, w0 + wpt);
+  int ce = 0;
+  for (int w = w0; w < w1; ++w) ce += __popc(eqm[w]);
+  int tot;
+  int eb = block_excl_scan(ce, sm, &tot);
+  int ck = 0, first_drop = N;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t e = eqm[w], sel = 0;
+    int allow = ntie - eb;
+    eb += __popc(e);
+    while (allow > 0 && e != 0u) {
+      const uint32_t b = e & (0u - e);
+      sel |= b;
+      e ^= b;
+      --allow;
+    }
+    const uint32_t kw = bm[w] | sel;
+    bm[w] = kw;
+    ck += __popc(kw);
+    const uint32_t valid = (w == W - 1 && (N & 31)) ? ((1u << (N & 31)) - 1u) : 0xffffffffu;
+    const uint32_t dropped = ~kw & valid;
+    if (dropped != 0u && first_drop == N) first_drop = 32 * w + __ffs(dropped) - 1;
+  }
+  int kb = block_excl_scan(ck, sm, &tot);
+  if (first_drop < N) atomicMin(&sm[56], first_drop);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t kw = bm[w];
+    while (kw != 0u) {
+      const int b = __ffs(kw) - 1;
+      kw &= kw - 1u;
+      if (kb < B) idx[kb] = 32 * w + b;
+      ++kb;
+    }
+  }
+  __syncthreads();
+  *e0_out = sm[56];
+  __syncthreads();
+  return true;
+}
+
+__device__ __forceinline__ bool select_one_pass_dispatch(const SCArgs &a, long long u, int N, const float *mom,
+                                                         uint32_t *hist, uint32_t *bm, uint32_t *eqm, int *sm,
+                                                         int *kept, int *e0) {
+  const float *raw_u = a.raw + u * a.G * a.capp;
+  uint2 *cand = reinterpret_cast<uint2 *>(a.keys + u * a.capp);   // the unit's key region, unused by this route
+  const int cap = a.capp / 2;
+  switch (a.G) {
+    case 1: return select_one_pass<1>(raw_u, N, a.budget, mom, hist, bm, eqm, sm, cand, cap, kept, e0);
+    case 2: return select_one_pass<2>(raw_u, N, a.budget, mom, hist, bm, eqm, sm, cand, cap, kept, e0);
+    case 4: return select_one_pass<4>(raw_u, N, a.budget, mom, hist, bm, eqm, sm, cand, cap, kept, e0);
+    default: return select_one_pass<8>(raw_u, N, a.budget, mom, hist, bm, eqm, sm, cand, cap, kept, e0);
+  }
+}
+
 __global__ void __launch_bounds__(kSelOnlyThreads, 4) select_only_kernel(const __grid_constant__ SCArgs a) {
-  __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist[4096];
+  __shared__ uint32_t bm[kBmMaxKeys / 32], eqm[kBmMaxKeys / 32];
   __shared__ int sm[kSelInts];
   __shared__ float mom[32];
   __shared__ int wc[3 * (kSelOnlyThreads / 32) + 1];
@@ -1545,6 +1972,14 @@ __global__ void __launch_bounds__(kSelOnlyThreads, 4) select_only_kernel(const _
     const int e0 = build_kept_gmem(keys, N, B, T, ntie, kept, sm);
     if (tid == 0) a.e0s[u] = e0;
     return;
+  }
+  if (N <= kBmMaxKeys) {
+    __syncthreads();
+    int e0 = N;
+    if (select_one_pass_dispatch(a, u, N, mom, hist, bm, eqm, sm, kept, &e0)) {
+      if (tid == 0) a.e0s[u] = e0;
+      return;
+    }
   }
   for (int b = tid; b < 256; b += nt) hist[b] = 0;
   __syncthreads();
@@ -1875,13 +2310,15 @@ static bool make_row_map(const tri_cache *c, void *base, CUtensorMap *map) {
 // {64, 128}): dense, a 2-D view [rows][d] with boxes of 64 elements x one
 // stage of rows; paged, the 4-D pool view with boxes of 64 elements x one block
 // of one head (a stage must hold a whole number of blocks, at most 32).
-static bool make_sw_map(const tri_cache *c, void *base, CUtensorMap *map) {
+// heads: KV heads per box (paged d = 128 only): 1, or every head of a block.
+static bool make_sw_map(const tri_cache *c, void *base, CUtensorMap *map, int heads = 1) {
   if (c->dtype != TRI_BF16 || (c->d != 64 && c->d != 128)) return false;
   const int rb = c->d * 2, tr = kStageBytes / rb;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr || base == nullptr) return false;
   CUresult r;
   if (c->block_table == nullptr) {
+    if (heads != 1) return false;
     const int64_t rows = (int64_t)c->L * c->S * c->Hkv * c->cap;
     if (rows >= (1ll << 31)) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)c->d, (cuuint64_t)rows};
@@ -1893,19 +2330,21 @@ static bool make_sw_map(const tri_cache *c, void *base, CUtensorMap *map) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else if (c->d == 128) {
     // 5-D view (64 elements, block rows, halves, heads, blocks) with a box of
-    // one block of one head, both halves: smem [half][block rows][128 B]
+    // one block of `heads` heads, both halves: smem [head][half][block rows][128 B]
     if (c->block > 256 || c->block % 8 != 0 || tr % c->block != 0 || tr / c->block > 32) return false;
+    if (heads != 1 && heads != c->Hkv) return false;
     if ((int64_t)c->L * c->nblocks >= (1ll << 31)) return false;
     const cuuint64_t dims[5] = {64u, (cuuint64_t)c->block, 2u, (cuuint64_t)c->Hkv,
                                 (cuuint64_t)c->L * (cuuint64_t)c->nblocks};
     const cuuint64_t strides[4] = {(cuuint64_t)c->Hkv * rb, 128u, (cuuint64_t)rb,
                                    (cuuint64_t)c->block * c->Hkv * rb};
-    const cuuint32_t box[5] = {64u, (cuuint32_t)c->block, 2u, 1u, 1u};
+    const cuuint32_t box[5] = {64u, (cuuint32_t)c->block, 2u, (cuuint32_t)heads, 1u};
     const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
     r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
+    if (heads != 1) return false;
     if (c->block > 256 || tr % c->block != 0 || tr / c->block > 32) return false;
     if ((int64_t)c->L * c->nblocks >= (1ll << 31)) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)c->d, (cuuint64_t)c->Hkv, (cuuint64_t)c->block,
@@ -2067,6 +2506,15 @@ static tri_status run_tiles(const TileArgs &a, int64_t units, cudaStream_t st) {
 // the CUDA-core tile kernel (head-major, one entry per tile).
 template <int D, int G, bool BF16>
 static tri_status run_keys(const TileArgs &a, int64_t units, cudaStream_t st) {
+  if constexpr (BF16 && D == 128) {
+    if (a.mma_ok && a.hg) {
+      const HgLayout lay(G, D / 2, a.c.Hkv);
+      auto k = score_heads_mma_kernel<G>;
+      if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
+      k<<<dim3((unsigned)a.ntiles, (unsigned)(a.c.L * a.c.S)), kHgThreads, lay.total, st>>>(a);
+      return launch_result();
+    }
+  }
   if constexpr (BF16) {
     if (a.mma_ok) {
       const KmLayout lay(G, D / 2);
@@ -2447,7 +2895,17 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   ta.raw_stride = sa.capp;
   ta.part = reinterpret_cast<float2 *>(static_cast<char *>(ws) + w.part_off);
   ta.phase = reinterpret_cast<const float2 *>(static_cast<char *>(ws) + w.phase_off);
-  if (ta.mma_ok) {   // key-major raw scores, one moment entry per CTA
+  // paged d = 128 caches whose block holds 128 head-rows: every KV head of a
+  // block in one copy (score_heads_mma_kernel)
+  ta.hg = ta.mma_ok && cache->block_table != nullptr && cache->d == 128 && cache->Hkv * cache->block == 128 &&
+          cache->block % 16 == 0 && (int64_t)cache->L * cache->S <= 65535 &&
+          HgLayout(G, cache->d / 2, cache->Hkv).total <= kMaxSmem && make_sw_map(cache, cache->k, &ta.ks, cache->Hkv);
+  if (ta.mma_ok && !ta.hg) ta.mma_ok = make_swizzled_map(cache, params, &ta.ks) ? 1 : 0;   // (the per-head map again)
+  if (ta.hg) {
+    ta.ntiles = (int)((cache->cap + kHgKeys - 1) / kHgKeys);
+    sa.raw_km = 1;
+    sa.part_keys = kHgKeys;
+  } else if (ta.mma_ok) {   // key-major raw scores, one moment entry per CTA
     ta.ntiles = (int)((cache->cap + kKmCtaKeys - 1) / kKmCtaKeys);
     sa.raw_km = 1;
     sa.part_keys = kKmCtaKeys;

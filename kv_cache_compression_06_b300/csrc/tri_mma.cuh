@@ -87,8 +87,11 @@ __device__ __forceinline__ void lds_v2(uint32_t (&r)[2], uint32_t addr) {
 // Called by all nc consumer threads (named barrier 1); for G == 8 the first
 // consumer warp (`writer`) then overwrites the start of wts with the lo trig
 // fragments (wts is dead once every consumer holds its fragments).
+// lo_dst (G == 8): where the lo fragments go instead of the start of wts
+// (12 x 32 lanes x 8 bytes), for callers whose wts region is reused after.
 template <int D, int G>
-__device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, float *wts, int nc, bool writer) {
+__device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, float *wts, int nc, bool writer,
+                                                 float *lo_dst = nullptr) {
   constexpr int F = D / 2;
   const int lane = threadIdx.x & 31, n = lane >> 2, k0 = 2 * (lane & 3);
   const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
@@ -138,7 +141,7 @@ __device__ __forceinline__ void load_mma_weights(MmaWeights<D, G> &w, float *wts
   }
   w.lo = 0;
   if constexpr (G == 8) {
-    uint2 *dst = reinterpret_cast<uint2 *>(wts);
+    uint2 *dst = reinterpret_cast<uint2 *>(lo_dst != nullptr ? lo_dst : wts);
     named_sync(1, nc);   // every consumer has read wts
     if (writer) {
 #pragma unroll

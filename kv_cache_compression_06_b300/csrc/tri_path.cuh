@@ -99,11 +99,15 @@ __device__ __forceinline__ float2 step_phase(const StepConst &sc, int f, int t) 
 // wts layout [G][3][F]: Re A, Im A, W for the G query heads of KV head g.
 // A_{h,f} = c_{h,f} * E_f with E_f the step phase of band f (computed here, or
 // taken from `phase` [F] when given); W_{h,f} = (1 - R_{h,f}) * m_{h,f}.
+// Threads [0, nthr) of the block take part (default: all).
 template <int G, int F>
 __device__ __forceinline__ void build_weights(float *wts, const float *center, const float *R,
                                               const float *mag, int Hq, int l, int g, int t,
-                                              const StepConst &sc, const float2 *phase = nullptr) {
-  for (int x = threadIdx.x; x < G * F; x += blockDim.x) {
+                                              const StepConst &sc, const float2 *phase = nullptr,
+                                              int nthr = 0) {
+  const int n = nthr > 0 ? nthr : (int)blockDim.x;
+  if ((int)threadIdx.x >= n) return;
+  for (int x = threadIdx.x; x < G * F; x += n) {
     const int h = x / F, f = x - h * F;
     const long long o = ((long long)l * Hq + (long long)g * G + h) * F + f;
     const float2 e = phase != nullptr ? phase[f] : step_phase(sc, f, t);

@@ -61,3 +61,11 @@ def test_fused_step_kernels(compact):
     w = WORKLOADS["qwen3_8b_36l_b16_n2176"]
     k = bench._step_kernels(w, 2176, compact, fused=True)
     assert k == ["fused_mma_kernel<128,4>"] + (["holefill_apply_kernel"] if compact == "holefill" else [])
+
+
+def test_paged_step_kernels_name_the_head_grouped_score_kernel():
+    w = WORKLOADS["qwen3_32b_64l_b64_paged"]
+    assert bench._step_kernels(w, 32768, "ordered", fused=False)[1] == "score_heads_mma_kernel"
+    assert bench._step_kernels(w.with_(block=32), 32768, "ordered", fused=False)[1] == "score_keys_mma_kernel"
+    assert bench._step_kernels(WORKLOADS["qwen3_8b_36l_b4_n32768"], 32768, "ordered", fused=False)[1] == \
+        "score_keys_mma_kernel"

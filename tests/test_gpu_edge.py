@@ -44,6 +44,13 @@ CASES = [
     W("edge_long_mma_g2_paged", Hq=4, n_range=(26000, 30000), budget=1024, paged=True, S=2),
     W("edge_long_mma_g8_paged32", Hq=16, n_range=(12000, 16000), budget=1024, paged=True, block=32),
     W("edge_long_cuda_f32_g2", Hq=4, d=64, dtype="f32", n_range=(30000, 40000), budget=2048, S=2),
+    # paged blocks of 128 head-rows (8 heads x 16 rows, 4 x 32): every KV head of
+    # a block scored by one CTA from one copy (score_heads_mma_kernel); lengths
+    # off the 2048-key CTA boundaries and partial last blocks
+    W("edge_long_hg_g8_h8_paged16", Hq=64, Hkv=8, n_range=(2100, 9000), budget=1024, paged=True, S=2),
+    W("edge_long_hg_g4_h8_paged16", Hq=32, Hkv=8, n_range=(4000, 14000), budget=2048, paged=True, S=2),
+    W("edge_long_hg_g1_h8_paged16", Hq=8, Hkv=8, n_range=(30000, 40000), budget=4096, paged=True, S=2),
+    W("edge_long_hg_g2_h4_paged32", Hq=8, Hkv=4, n_range=(30000, 36000), budget=2048, paged=True, block=32, S=2),
     W("edge_long_cuda_inter_g4", Hq=8, pairing="interleaved", n_range=(11000, 14000), budget=1024),
     # linear future offsets instead of geometric ones
     W("edge_linear_offsets_fused_g4", Hq=8, n_range=(600, 1800), budget=700, offsets=LIN32),

@@ -64,6 +64,7 @@ CASES = [
     W("guard_fused_paged32_d64_g2", Hq=4, d=64, n_range=(300, 1900), paged=True, block=32),
     W("guard_long_dense_g4", n_range=(400, 13000), budget=1024),
     W("guard_long_paged_g8", Hq=16, n_range=(400, 16000), budget=1000, paged=True),
+    W("guard_long_paged_hg_g4_h8", Hq=32, Hkv=8, n_range=(400, 9000), budget=1000, paged=True, S=3),
     W("guard_long_f32_d64", d=64, dtype="f32", n_range=(20000, 30000), budget=2000, S=2),
 ]
 
