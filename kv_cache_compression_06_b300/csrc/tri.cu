@@ -258,9 +258,26 @@ __device__ __forceinline__ Pipe make_pipe(char *smem, int bars) {
 // E[s][f] = e^{i*omega_f*t_s} * Phi_f for every sequence and band, once per call
 // (the tile CTAs of a unit all need it; computing it per tile cost ~20
 // instructions per key at G = 8).
-__global__ void __launch_bounds__(64) phase_kernel(const int *t, int F, float2 *phase, const StepConst sc) {
+// Also, when `order` is given, the sequences ranked by length, longest first
+// (ties by index): order[rank] = s.  The long-unit selection takes its units
+// in that order, so that the longest ones do not start in the last wave.
+__global__ void __launch_bounds__(64) phase_kernel(const int *t, int F, float2 *phase, const StepConst sc,
+                                                   const int *seq_len, int S, int *order) {
   const int s = blockIdx.x;
   for (int f = threadIdx.x; f < F; f += blockDim.x) phase[(long long)s * F + f] = step_phase(sc, f, t[s]);
+  if (order != nullptr) {
+    __shared__ int part[2];
+    const int n = seq_len[s];
+    int r = 0;
+    for (int x = threadIdx.x; x < S; x += blockDim.x) {
+      const int m = seq_len[x];
+      r += (m > n) || (m == n && x < s);
+    }
+    r = warp_sum_int(r);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = r;
+    __syncthreads();
+    if (threadIdx.x == 0) order[part[0] + part[1]] = s;
+  }
 }
 
 // ---------------------------------------------------------------- long units: tiles
@@ -275,6 +292,7 @@ struct TileArgs {
   int hg;            // ks boxes every KV head of a block: score_heads_mma_kernel
   long long raw_stride;
   const float2 *phase;   // [S][F] step phases (phase_kernel); raw_stride: floats between the raw rows of two heads (cap, or capp in the workspace)
+  int *order;            // [S] sequences by length, longest first (phase_kernel), or null
   float *raw;      // [(u*G + h)*raw_stride + i]
   float2 *part;    // [(u*ntiles + tile)*G + h] = (mean, M2) of the tile
   StepConst sc;
@@ -1055,7 +1073,7 @@ __global__ void __launch_bounds__(kThreads, 2) score_keys_mma_kernel(const __gri
 // slots' full barriers in turn, and a parity wait cannot match a phase two
 // back (a slot shared by both parities would let a warp that ran a cycle
 // ahead see the previous use's completed phase as its own).
-constexpr int kHgKeys = 2048;       // keys per CTA and head (one part entry)
+constexpr int kHgKeys = 4096;       // keys per CTA and head (one part entry)
 constexpr int kHgStages = 6;
 constexpr int kHgEarly = 4;         // stages issued before the weights are taken
 static_assert(kHgStages % 2 == 0, "ring slots must belong to one consumer parity");
@@ -1250,6 +1268,7 @@ struct SCArgs {
   int part_keys;    // mode 0: keys covered by one (mean, M2) entry of part
   int *kept;        // select_only / compact_only: kept slots [units][budget] (idx_out or workspace)
   int *e0s;         // select_only / compact_only: first dropped slot per unit (workspace)
+  const int *order; // select_only: sequences longest first (its CTAs take units in that order), or null
 };
 
 // The keys (one u32 per slot) and the compaction ring share one region at the
@@ -1947,7 +1966,11 @@ __global__ void __launch_bounds__(kSelOnlyThreads, 4) select_only_kernel(const _
   __shared__ int wc[3 * (kSelOnlyThreads / 32) + 1];
   const CacheView &c = a.c;
   const int tid = threadIdx.x, nt = blockDim.x;
-  const int u = blockIdx.x;
+  int u = blockIdx.x;
+  if (a.order != nullptr) {   // CTA i takes the units of the (i / (L Hkv))-th longest sequence
+    const int per = c.L * c.Hkv, rem = u % per;
+    u = ((rem / c.Hkv) * c.S + a.order[u / per]) * c.Hkv + rem % c.Hkv;
+  }
   const int g = u % c.Hkv, s = (u / c.Hkv) % c.S, l = u / (c.Hkv * c.S);
   if (timed_out()) return;
   const int N = c.seq_len[s];
@@ -2399,7 +2422,7 @@ static bool fused_fits(const tri_cache *c, int G) {
 }
 
 struct SplitWs {
-  size_t raw_off, part_off, phase_off, keys_off, kept_off, e0_off, total;
+  size_t raw_off, part_off, phase_off, keys_off, kept_off, e0_off, order_off, total;
 };
 static SplitWs split_ws(const tri_cache *c, int G, int budget) {
   SplitWs w;
@@ -2417,7 +2440,8 @@ static SplitWs split_ws(const tri_cache *c, int G, int budget) {
   const size_t e0 = (size_t)units_of(c) * sizeof(int);
   w.kept_off = w.keys_off + (keys + 255) / 256 * 256;
   w.e0_off = w.kept_off + (kept + 255) / 256 * 256;
-  w.total = w.e0_off + (e0 + 255) / 256 * 256;
+  w.order_off = w.e0_off + (e0 + 255) / 256 * 256;   // sequences by length (S ints)
+  w.total = w.order_off + ((size_t)c->S * sizeof(int) + 255) / 256 * 256;
   return w;
 }
 
@@ -2427,7 +2451,8 @@ static tri_status launch_result() {
 
 // Fills the workspace's step phases (before the tile kernels).
 static tri_status run_phases(const tri_cache *c, const TileArgs &ta, cudaStream_t st) {
-  phase_kernel<<<(unsigned)c->S, 64, 0, st>>>(ta.t, c->d / 2, const_cast<float2 *>(ta.phase), ta.sc);
+  phase_kernel<<<(unsigned)c->S, 64, 0, st>>>(ta.t, c->d / 2, const_cast<float2 *>(ta.phase), ta.sc, c->seq_len,
+                                               (int)c->S, ta.order);
   return launch_result();
 }
 
@@ -2937,6 +2962,12 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   if (split) {
     sa.kept = ((!sa.holefill || apply) && idx_out != nullptr) ? idx_out : reinterpret_cast<int *>(wsb + w.kept_off);
     sa.e0s = reinterpret_cast<int *>(wsb + w.e0_off);
+    // longest sequences first in the selection (ranked by phase_kernel; the
+    // ranking costs S per sequence, so only for S up to 4096)
+    if (cache->S <= 4096) {
+      ta.order = reinterpret_cast<int *>(wsb + w.order_off);
+      sa.order = ta.order;
+    }
   }
   if ((e = run_phases(cache, ta, stream)) != TRI_OK) return e;
   if ((e = TRI_DISPATCH(run_keys, cache->d, G, bf16, ta, units, stream)) != TRI_OK) return e;
