@@ -1107,7 +1107,7 @@ __global__ void __launch_bounds__(kHgThreads, 1) score_heads_mma_kernel(const __
   float *lo = reinterpret_cast<float *>(smem + lay.lo);
   float *red = reinterpret_cast<float *>(smem + lay.red);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ls = blockIdx.y;
+  const int ls = blockIdx.y, chunk = blockIdx.x;
   const int s = ls % c.S, l = ls / c.S;
   if (timed_out()) return;
   const int N = c.seq_len[s];
@@ -1116,7 +1116,7 @@ __global__ void __launch_bounds__(kHgThreads, 1) score_heads_mma_kernel(const __
     return;
   }
   if (a.skip_small && N <= a.budget) return;
-  const int i0 = blockIdx.x * kHgKeys;
+  const int i0 = chunk * kHgKeys;
   if (i0 >= N) return;
   const int n = min(kHgKeys, N - i0);
   if (!c.blocks_ok(s, n, i0)) {
@@ -1218,7 +1218,7 @@ __global__ void __launch_bounds__(kHgThreads, 1) score_heads_mma_kernel(const __
       chan_merge(nn, mm, qq, rw[0], rw[1 + j], rw[3 + j]);
     }
     const long long u = (long long)ls * c.Hkv + h;
-    a.part[((long long)u * a.ntiles + blockIdx.x) * G + qh] = make_float2(mm, qq);
+    a.part[((long long)u * a.ntiles + chunk) * G + qh] = make_float2(mm, qq);
   }
 }
 
@@ -1725,9 +1725,30 @@ __device__ __noinline__ int select_rest_candidates(const uint32_t *keys, int n, 
 constexpr int kSampleKeys = 1024;
 constexpr int kBmMaxKeys = 65536;   // bitmask words in shared memory: 2 x 8 KB
 
+// Key i's G raw scores (key-major rows, 16-byte aligned for G >= 4).
 template <int G>
-__device__ __forceinline__ uint32_t zkey_of(const float *raw_u, int i, const float *mu, const float *iv) {
-  const float *x = raw_u + (long long)i * G;
+__device__ __forceinline__ void load_key_scores(const float *raw_u, int i, float (&x)[G]) {
+  const float *p = raw_u + (long long)i * G;
+  if constexpr (G % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < G / 4; ++q) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(p) + q);
+      x[4 * q] = v.x;
+      x[4 * q + 1] = v.y;
+      x[4 * q + 2] = v.z;
+      x[4 * q + 3] = v.w;
+    }
+  } else if constexpr (G == 2) {
+    const float2 v = __ldg(reinterpret_cast<const float2 *>(p));
+    x[0] = v.x;
+    x[1] = v.y;
+  } else {
+    x[0] = __ldg(p);
+  }
+}
+
+template <int G>
+__device__ __forceinline__ uint32_t zkey_from(const float (&x)[G], const float *mu, const float *iv) {
   float z = (x[0] - mu[0]) * iv[0];
 #pragma unroll
   for (int h = 1; h < G; ++h) z = fmaxf(z, (x[h] - mu[h]) * iv[h]);
@@ -1793,11 +1814,19 @@ __device__ __noinline__ bool select_one_pass(const float *raw_u, int N, int B, c
     sm[50] = 0;   // candidate overflow
   }
   __syncthreads();
-  // the sample
+  // the sample: every thread's keys loaded before any is used
   const int ns = min(kSampleKeys, N);
-  for (int j = tid; j < ns; j += nt) {
-    const int i = (int)(((long long)j * N) / ns);
-    atomicAdd(&hist[zkey_of<G>(raw_u, i, mu, iv) >> 20], 1u);
+  {
+    constexpr int SPT = kSampleKeys / kSelOnlyThreads;
+    float x[SPT][G];
+#pragma unroll
+    for (int k = 0; k < SPT; ++k) {
+      const int j = tid + k * nt;
+      if (j < ns) load_key_scores<G>(raw_u, (int)(((long long)j * N) / ns), x[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < SPT; ++k)
+      if (tid + k * nt < ns) atomicAdd(&hist[zkey_from<G>(x[k], mu, iv) >> 20], 1u);
   }
   __syncthreads();
   const float p = (float)B / (float)N;
@@ -1877,10 +1906,12 @@ __device__ __noinline__ bool select_one_pass(const float *raw_u, int N, int B, c
     __syncthreads();
     return false;
   }
-  // T: the k_in-th largest candidate
-  uint32_t prefix = 0, mask = 0;
+  // T: the k_in-th largest candidate (its top 8 bits are known when the
+  // range's digits share them)
+  const bool top_known = (d_lo >> 4) == (d_hi >> 4);
+  uint32_t prefix = top_known ? (d_lo >> 4) << 24 : 0u, mask = top_known ? 0xff000000u : 0u;
   int k = k_in;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int shift = top_known ? 16 : 24; shift >= 0; shift -= 8) {
     for (int b = tid; b < 256; b += nt) hist[b] = 0;
     __syncthreads();
     for (int x = tid; x < c; x += nt) {
