@@ -116,8 +116,8 @@ struct FusedArgs {
   const int *t;
   int budget, mode, inter, capp;   // mode 0: compress, 1: score only
   int holefill;                    // compaction layout: 0 ordered, 1 hole-fill
-  int defer;                       // hole-fill: write the ascending kept list to idx_out
-                                   // and leave the rows to holefill_apply_kernel
+  int defer;                       // hole-fill: write the kept set to idx_out as a bitmask
+                                   // and leave the layout and rows to holefill_apply_kernel
   int mma_ok;                      // host only: try the tensor-core variant
   const tri_cache *cache;          // host only: for that variant's tensor map
   const tri_params *params;
@@ -226,15 +226,18 @@ __global__ void __launch_bounds__(kFusedThreads, (G <= 4 ? 2 : 1)) fused_kernel(
   __syncthreads();
   int ntie;
   const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
+  if (a.defer) {   // hole-fill: the kept set as a bitmask in idx_out; holefill_apply_kernel does the rest
+    kept_bits(keys, N, T, ntie, reinterpret_cast<uint32_t *>(a.idx_out + (long long)u * B), sm);
+    return;
+  }
   const int e0 = build_kept_chunked(keys, N, B, T, ntie, idxs, sm);
-  if (a.holefill && !a.defer) {   // keys are dead: their 4N bytes hold the hole-fill bookkeeping
+  if (a.holefill) {   // keys are dead: their 4N bytes hold the hole-fill bookkeeping
     holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), ring, kRingBytes, sm,
                   a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
     return;
   }
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
-  if (a.holefill) return;   // holefill_apply_kernel moves the rows
   // The ring was last read by generic loads (scoring); TMA writes it next.
   fence_proxy_async_smem();
   __syncthreads();
@@ -823,15 +826,18 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 2 : 1))
   __syncthreads();
   int ntie;
   const uint32_t T = radix_select_atomic(keys, N, B, hist, sm, &ntie);
+  if (a.defer) {   // hole-fill: the kept set as a bitmask in idx_out; holefill_apply_kernel does the rest
+    kept_bits(keys, N, T, ntie, reinterpret_cast<uint32_t *>(a.idx_out + (long long)u * B), sm);
+    return;
+  }
   const int e0 = build_kept_chunked(keys, N, B, T, ntie, idxs, sm);
-  if (a.holefill && !a.defer) {
+  if (a.holefill) {
     holefill_unit(c, l, s, g, idxs, B, N, reinterpret_cast<char *>(keys), ring, kRingBytes, sm,
                   a.idx_out != nullptr ? a.idx_out + (long long)u * B : nullptr);
     return;
   }
   if (a.idx_out != nullptr)
     for (int j = tid; j < B; j += nt) a.idx_out[(long long)u * B + j] = idxs[j];
-  if (a.holefill) return;   // holefill_apply_kernel moves the rows
   // The ring was last read by ldmatrix (generic proxy); TMA writes it next.
   fence_proxy_async_smem();
   __syncthreads();
@@ -2142,7 +2148,9 @@ constexpr int kHfBatch = 4;
 struct HfArgs {
   CacheView c;
   int budget;
-  const int *kept;   // [units][B] ascending kept slots (may alias idx_out)
+  const int *kept;   // [units][B] ascending kept slots, or (from_bits) the kept bitmask in
+                     // the first ceil(N / 32) words of the unit's row; may alias idx_out
+  int from_bits;
   int *idx_out;      // [units][B] or null: the layout (original slot now at j)
   int *new_len;      // [S] or null
   int outputs;       // 1: also the lengths and the identity idx of units with N <= B
@@ -2182,9 +2190,34 @@ __global__ void __launch_bounds__(kHfThreads, 4) holefill_apply_kernel(const __g
   }
   int *list = hsm, *holes = hsm + B;
   const int *src = a.kept + (long long)u * B;
-  for (int j = tid; j < B; j += nt) list[j] = src[j];
-  __syncthreads();
   int bad = 0;
+  if (a.from_bits) {   // the kept slots are the set bits, in order: a scan of the words' counts
+    __shared__ int scan[32];
+    const uint32_t *bits = reinterpret_cast<const uint32_t *>(src);
+    const int W = (N + 31) / 32, wpt = (W + nt - 1) / nt;
+    const int w0 = min(W, tid * wpt), w1 = min(W, w0 + wpt);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) {
+      const uint32_t b = bits[w];
+      cnt += __popc(b);
+      if (w == W - 1 && (N & 31) != 0) bad |= (b >> (N & 31)) != 0u;   // no bit at or past N
+    }
+    int tot;
+    int pos = block_excl_scan(cnt, scan, &tot);
+    bad |= tot != B;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t b = bits[w];
+      while (b != 0u) {
+        const int i = __ffs(b) - 1;
+        b &= b - 1u;
+        if (pos < B) list[pos] = 32 * w + i;
+        ++pos;
+      }
+    }
+  } else {
+    for (int j = tid; j < B; j += nt) list[j] = src[j];
+  }
+  __syncthreads();
   for (int j = tid; j < B; j += nt) bad |= (list[j] < 0) | (list[j] >= N) | (j > 0 && list[j] <= list[j - 1]);
   if (__syncthreads_or(bad)) {   // every read of the list in global memory is done
     if (tid == 0) set_status(TRI_ERR_INVALID);
@@ -2500,13 +2533,14 @@ static tri_status set_smem(K kernel, int bytes) {
 constexpr int kHfMaxSmem = 57344;
 static bool hf_apply_ok(int B) { return hf_apply_smem(B) <= kHfMaxSmem; }
 
-static tri_status run_holefill_apply(const CacheView &view, int B, const int *kept, int32_t *idx_out,
+static tri_status run_holefill_apply(const CacheView &view, int B, const int *kept, int from_bits, int32_t *idx_out,
                                      int32_t *new_len, int outputs, int64_t units, cudaStream_t st) {
   HfArgs h;
   std::memset(&h, 0, sizeof(h));
   h.c = view;
   h.budget = B;
   h.kept = kept;
+  h.from_bits = from_bits;
   h.idx_out = idx_out;
   h.new_len = new_len;
   h.outputs = outputs;
@@ -2923,13 +2957,15 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
     FusedArgs a = fused_args(cache, stats, params);
     a.mode = 0;
     a.holefill = mode == TRI_COMPACT_HOLEFILL;
-    // hole-fill: the fused kernel selects and writes the kept list to idx_out,
-    // holefill_apply_kernel turns it into the layout and moves the rows
-    a.defer = a.holefill && idx_out != nullptr && hf_apply_ok(params->budget);
+    // hole-fill: the fused kernel selects and writes the kept set to idx_out as a
+    // bitmask (ceil(cap / 32) <= B words), holefill_apply_kernel turns it into
+    // the layout and moves the rows
+    a.defer = a.holefill && idx_out != nullptr && hf_apply_ok(params->budget) &&
+              (cache->cap + 31) / 32 <= params->budget;
     a.idx_out = idx_out;
     a.new_len = new_len;
     if ((e = TRI_DISPATCH(run_fused, cache->d, G, bf16, a, units, stream)) != TRI_OK || !a.defer) return e;
-    return run_holefill_apply(a.c, params->budget, idx_out, idx_out, new_len, 0, units, stream);
+    return run_holefill_apply(a.c, params->budget, idx_out, 1, idx_out, new_len, 0, units, stream);
   }
   const SplitWs w = split_ws(cache, G, params->budget);
   if (ws == nullptr || ws_bytes < w.total || !aligned16(ws)) return TRI_ERR_WORKSPACE;
@@ -3005,7 +3041,7 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
   if (!split) return run_select_compact(sa, units, stream);
   select_only_kernel<<<(unsigned)units, kSelOnlyThreads, 0, stream>>>(sa);
   if ((e = launch_result()) != TRI_OK) return e;
-  if (apply) return run_holefill_apply(sa.c, params->budget, sa.kept, idx_out, new_len, 1, units, stream);
+  if (apply) return run_holefill_apply(sa.c, params->budget, sa.kept, 0, idx_out, new_len, 1, units, stream);
   if (set_smem(compact_only_kernel, co.total) != TRI_OK) return TRI_ERR_CUDA;
   compact_only_kernel<<<(unsigned)units, kCoThreads, co.total, stream>>>(sa);
   return launch_result();

@@ -652,6 +652,40 @@ __device__ __noinline__ int build_kept(const uint32_t *keys, int n, int K, uint3
   return e0;
 }
 
+// Writes the kept set of keys[0..n) (those > T, plus the first ntie equal to
+// T in slot order) as a bitmask: bit i % 32 of out[i / 32] (bits of slots at or
+// past n are 0).  Each warp owns a contiguous run of 32-slot words; a block
+// scan of the warps' counts of keys equal to T allots the ties in slot order.
+// sm: 32 ints for the scan.
+__device__ __noinline__ void kept_bits(const uint32_t *keys, int n, uint32_t T, int ntie, uint32_t *out, int *sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int W = (n + 31) / 32, wpw = (W + nw - 1) / nw;
+  const int w0 = min(W, warp * wpw), w1 = min(W, w0 + wpw);
+  int ceq = 0;
+  for (int w = w0; w < w1; ++w) {
+    const int i = 32 * w + lane;
+    ceq += __popc(__ballot_sync(0xffffffffu, i < n && keys[i] == T));
+  }
+  int tot;
+  int before = block_excl_scan(lane == 0 ? ceq : 0, sm, &tot);
+  before = __shfl_sync(0xffffffffu, before, 0);
+  int allow = ntie - before;   // ties this warp may still keep (warp-uniform)
+  for (int w = w0; w < w1; ++w) {
+    const int i = 32 * w + lane;
+    const bool in = i < n;
+    const uint32_t k = in ? keys[i] : 0u;
+    const uint32_t gt = __ballot_sync(0xffffffffu, in && k > T);
+    uint32_t eq = __ballot_sync(0xffffffffu, in && k == T), sel = 0;
+    while (allow > 0 && eq != 0u) {
+      const uint32_t b = eq & (0u - eq);
+      sel |= b;
+      eq ^= b;
+      --allow;
+    }
+    if (lane == 0) out[w] = gt | sel;
+  }
+}
+
 // ---------------------------------------------------------------- top-B over keys in global memory
 // Variants of radix_select_atomic / build_kept for keys stored in global memory
 // (L2-resident: one unit's keys are 4 N bytes), used by the long-unit select
