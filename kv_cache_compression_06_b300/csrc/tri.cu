@@ -18,10 +18,13 @@
 //   score_keys_mma_kernel a1+a2 of the compress step for long bf16 units:
 //                        key-major raw scores straight from the MMA fragments,
 //                        moments in registers, one (mean, M2) per CTA.
-//   select_only_kernel   a3+a4 of the compress step for long units: kept slots.
+//   score_heads_mma_kernel the same for paged caches whose block holds 128
+//                        head-rows: every KV head of a block from one copy.
+//   select_only_kernel   a3+a4 of the compress step for long units: kept slots
+//                        (one pass over the raw scores, or the full passes).
 //   compact_only_kernel  a5 of the compress step for long units.
-//   holefill_apply_kernel a5 in the hole-fill layout after any selection that
-//                        wrote ascending kept lists: layout + independent row moves.
+//   holefill_apply_kernel a5 in the hole-fill layout after a selection that
+//                        wrote kept lists or bitmasks: layout + independent row moves.
 //   zmax_kernel          a3 for long units (tri_score): Chan-merged moments -> agg.
 //   select_compact_kernel a3..a5 for long units whose kept list or hole-fill
 //                        bookkeeping does not fit compact_only_kernel,
@@ -1725,9 +1728,10 @@ __device__ __noinline__ int select_rest_candidates(const uint32_t *keys, int n, 
 // first ntie in slot order join the kept set; a scan over the words writes
 // the kept slots in ascending order.  Same result as the full passes (kept =
 // keys > T, then the first ntie keys equal to T in slot order); the raw scores
-// are read once and no key array is written.  Returns false, with nothing
-// written, when the sample's range missed T or the candidates overflow: the
-// caller then runs the full passes.
+// are read once and no key array is written.  Returns false, with no output
+// written (only shared memory and the unit's key region touched), when the
+// sample's range missed T or the candidates overflow: the caller then runs the
+// full passes.
 constexpr int kSampleKeys = 1024;
 constexpr int kBmMaxKeys = 65536;   // bitmask words in shared memory: 2 x 8 KB
 
@@ -2129,9 +2133,10 @@ __global__ void __launch_bounds__(kCoThreads, 2) compact_only_kernel(const __gri
 }
 
 // ---------------------------------------------------------------- hole-fill moves
-// Hole-fill compaction of every unit from its ascending kept list, written by
-// the selection (the fused kernel or select_only_kernel) earlier in the step.
-// Layout: the kept slots below B stay; the r-th evicted slot below B (hole r)
+// Hole-fill compaction of every unit from its kept set, written by the
+// selection earlier in the step: as the ascending kept list (select_only_kernel)
+// or as a bitmask (the fused kernel), from which a scan of the words' counts
+// builds the list in shared memory.  Layout: the kept slots below B stay; the r-th evicted slot below B (hole r)
 // receives the r-th kept slot at or above B (mover r).  A slot finds its
 // source without a scan: with P kept slots below B and kb of them below j
 // (binary search in the list's head), slot j is kept iff list[kb] == j, else it

@@ -95,6 +95,36 @@ def test_all_zero_keys_tie_everywhere(n_keys, Hq):
     C.run_and_check(w, generate(w, device=DEV), [(0, 0, 0)], DEV)
 
 
+def test_long_unit_top_keys_off_the_sampled_slots():
+    """The long-unit selection brackets the threshold with a sample of every
+    (N / 1024)-th slot.  A unit's score depends only on the stored (post-RoPE)
+    row, not on its slot, so moving the rows of the B highest aggregated scores
+    onto slots the sample never reads hides them from it: its range then sits
+    below the threshold and the selection must notice and take its full passes.
+    Parity with the oracle as for every unit (both KV heads; head 0 moved)."""
+    import kv_cache_compression_06_b300 as tk
+    N, B = 20000, 300
+    w = W("edge_sample_miss_g4", Hq=8, S=1, Hkv=2, budget=B, n_keys=N)
+    data = generate(w, device=DEV)
+    cache, stats, params = C.setup(w, data, DEV)
+    probe = tk.KVCache(cache.k.clone(), cache.v.clone(), cache.seq_len, Hkv=w.Hkv)
+    agg = torch.zeros((1, 1, w.Hkv, w.cap), dtype=torch.float32, device=DEV)
+    tk.tri_score(probe, stats, params, agg=agg)
+    a = agg[0, 0, 0, :N].double().cpu().numpy()
+    top = np.argsort(-a, kind="stable")[:B]
+    sampled = {(j * N) // 1024 for j in range(1024)}
+    free = np.array([i for i in range(N) if i not in sampled])
+    rest = np.array([i for i in range(N) if i not in set(top.tolist())])
+    order = np.empty(N, dtype=np.int64)          # order[slot] = original row now at slot
+    order[free[:B]] = top
+    others = np.array([i for i in range(N) if i not in set(free[:B].tolist())])
+    order[others] = rest
+    perm = torch.as_tensor(order, device=DEV)
+    for t in ("k", "v"):
+        data[t][0, 0, 0, :N] = data[t][0, 0, 0, :N][perm].clone()
+    C.run_and_check(w, data, [(0, 0, 0), (0, 0, 1)], DEV)
+
+
 HOLEFILL_CASES = [
     W("hf_fused_g4", Hq=8, n_range=(600, 1900), budget=700),
     W("hf_fused_paged_g2_d64", Hq=4, d=64, n_range=(700, 2500), paged=True),
