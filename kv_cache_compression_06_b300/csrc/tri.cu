@@ -264,25 +264,67 @@ __device__ __forceinline__ Pipe make_pipe(char *smem, int bars) {
 // E[s][f] = e^{i*omega_f*t_s} * Phi_f for every sequence and band, once per call
 // (the tile CTAs of a unit all need it; computing it per tile cost ~20
 // instructions per key at G = 8).
+// Sum over the block (64 threads) of v; every thread gets it.
+__device__ __forceinline__ int sum64(int v, int *part) {
+  v = warp_sum_int(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return part[0] + part[1];
+}
+
 // Also, when `order` is given, the sequences ranked by length, longest first
 // (ties by index): order[rank] = s.  The long-unit selection takes its units
 // in that order, so that the longest ones do not start in the last wave.
+// When `plan` is given, the chunk plan of the head-grouped score kernel
+// (chunks of `ck` keys of the sequences with budget < N <= cap): plan[0] = full
+// chunks per layer, plan[1] = sequences with a partial last chunk,
+// plan[2 + s] = full chunks of the sequences before s, plan[2 + S + r] = the
+// sequence with the r-th largest partial chunk (ties by index).  The score
+// kernel runs the full chunks first and the partial ones last, largest first,
+// so that the last wave holds the smallest CTAs.
 __global__ void __launch_bounds__(64) phase_kernel(const int *t, int F, float2 *phase, const StepConst sc,
-                                                   const int *seq_len, int S, int *order) {
+                                                   const int *seq_len, int S, int *order, int *plan, int budget,
+                                                   long long cap, int ck) {
+  __shared__ int part[2];
   const int s = blockIdx.x;
   for (int f = threadIdx.x; f < F; f += blockDim.x) phase[(long long)s * F + f] = step_phase(sc, f, t[s]);
   if (order != nullptr) {
-    __shared__ int part[2];
     const int n = seq_len[s];
     int r = 0;
     for (int x = threadIdx.x; x < S; x += blockDim.x) {
       const int m = seq_len[x];
       r += (m > n) || (m == n && x < s);
     }
-    r = warp_sum_int(r);
-    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = r;
-    __syncthreads();
-    if (threadIdx.x == 0) order[part[0] + part[1]] = s;
+    r = sum64(r, part);
+    if (threadIdx.x == 0) order[r] = s;
+  }
+  if (plan != nullptr) {
+    auto live = [&](int m) { return m > budget && (long long)m <= cap; };
+    const int n = seq_len[s], rem = live(n) ? n % ck : 0;
+    int before = 0, tot_full = 0, tot_part = 0, rank = 0;
+    for (int x = threadIdx.x; x < S; x += blockDim.x) {
+      const int m = seq_len[x];
+      const int fx = live(m) ? m / ck : 0, rx = live(m) ? m % ck : 0;
+      if (x < s) before += fx;
+      tot_full += fx;
+      tot_part += rx > 0;
+      rank += rx > 0 && (rx > rem || (rx == rem && x < s));
+    }
+    before = sum64(before, part);
+    if (s == 0) {
+      tot_full = sum64(tot_full, part);
+      tot_part = sum64(tot_part, part);
+    }
+    rank = sum64(rank, part);
+    if (threadIdx.x == 0) {
+      plan[2 + s] = before;
+      if (rem > 0) plan[2 + S + rank] = s;
+      if (s == 0) {
+        plan[0] = tot_full;
+        plan[1] = tot_part;
+      }
+    }
   }
 }
 
@@ -299,6 +341,7 @@ struct TileArgs {
   long long raw_stride;
   const float2 *phase;   // [S][F] step phases (phase_kernel); raw_stride: floats between the raw rows of two heads (cap, or capp in the workspace)
   int *order;            // [S] sequences by length, longest first (phase_kernel), or null
+  int *plan;             // [2 S + 2] chunk plan of score_heads_mma_kernel (phase_kernel), or null
   float *raw;      // [(u*G + h)*raw_stride + i]
   float2 *part;    // [(u*ntiles + tile)*G + h] = (mean, M2) of the tile
   StepConst sc;
@@ -1116,7 +1159,34 @@ __global__ void __launch_bounds__(kHgThreads, 1) score_heads_mma_kernel(const __
   float *lo = reinterpret_cast<float *>(smem + lay.lo);
   float *red = reinterpret_cast<float *>(smem + lay.red);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ls = blockIdx.y, chunk = blockIdx.x;
+  int ls, chunk;
+  if (a.plan != nullptr) {   // 1-D grid over the chunk plan: full chunks, then partial ones, largest first
+    const int nfull = a.plan[0], npart = a.plan[1];
+    const long long i = blockIdx.x, nf = (long long)c.L * nfull;
+    int ll, sq;
+    if (i < nf) {
+      ll = (int)(i / nfull);
+      const int k = (int)(i % nfull);
+      int lo = 0, hi = c.S - 1;   // the last sequence whose full chunks start at or before k
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.plan[2 + mid] <= k) lo = mid; else hi = mid - 1;
+      }
+      sq = lo;
+      chunk = k - a.plan[2 + lo];
+    } else if (i < nf + (long long)c.L * npart) {
+      const long long j = i - nf;
+      ll = (int)(j % c.L);
+      sq = a.plan[2 + c.S + (int)(j / c.L)];
+      chunk = c.seq_len[sq] / kHgKeys;
+    } else {
+      return;
+    }
+    ls = ll * c.S + sq;
+  } else {
+    ls = blockIdx.y;
+    chunk = blockIdx.x;
+  }
   const int s = ls % c.S, l = ls / c.S;
   if (timed_out()) return;
   const int N = c.seq_len[s];
@@ -2491,7 +2561,7 @@ static bool fused_fits(const tri_cache *c, int G) {
 }
 
 struct SplitWs {
-  size_t raw_off, part_off, phase_off, keys_off, kept_off, e0_off, order_off, total;
+  size_t raw_off, part_off, phase_off, keys_off, kept_off, e0_off, order_off, plan_off, total;
 };
 static SplitWs split_ws(const tri_cache *c, int G, int budget) {
   SplitWs w;
@@ -2510,7 +2580,8 @@ static SplitWs split_ws(const tri_cache *c, int G, int budget) {
   w.kept_off = w.keys_off + (keys + 255) / 256 * 256;
   w.e0_off = w.kept_off + (kept + 255) / 256 * 256;
   w.order_off = w.e0_off + (e0 + 255) / 256 * 256;   // sequences by length (S ints)
-  w.total = w.order_off + ((size_t)c->S * sizeof(int) + 255) / 256 * 256;
+  w.plan_off = w.order_off + ((size_t)c->S * sizeof(int) + 255) / 256 * 256;   // chunk plan (2 S + 2 ints)
+  w.total = w.plan_off + ((size_t)(2 * c->S + 2) * sizeof(int) + 255) / 256 * 256;
   return w;
 }
 
@@ -2521,7 +2592,7 @@ static tri_status launch_result() {
 // Fills the workspace's step phases (before the tile kernels).
 static tri_status run_phases(const tri_cache *c, const TileArgs &ta, cudaStream_t st) {
   phase_kernel<<<(unsigned)c->S, 64, 0, st>>>(ta.t, c->d / 2, const_cast<float2 *>(ta.phase), ta.sc, c->seq_len,
-                                               (int)c->S, ta.order);
+                                               (int)c->S, ta.order, ta.plan, ta.budget, (long long)c->cap, kHgKeys);
   return launch_result();
 }
 
@@ -2606,7 +2677,9 @@ static tri_status run_keys(const TileArgs &a, int64_t units, cudaStream_t st) {
       const HgLayout lay(G, D / 2, a.c.Hkv);
       auto k = score_heads_mma_kernel<G>;
       if (set_smem(k, lay.total) != TRI_OK) return TRI_ERR_CUDA;
-      k<<<dim3((unsigned)a.ntiles, (unsigned)(a.c.L * a.c.S)), kHgThreads, lay.total, st>>>(a);
+      const dim3 grid = a.plan != nullptr ? dim3((unsigned)((long long)a.c.L * a.c.S * a.ntiles))
+                                          : dim3((unsigned)a.ntiles, (unsigned)(a.c.L * a.c.S));
+      k<<<grid, kHgThreads, lay.total, st>>>(a);
       return launch_result();
     }
   }
@@ -3039,6 +3112,8 @@ tri_status tri_compress_step(const tri_cache *cache, const tri_stats *stats,
     if (cache->S <= 4096) {
       ta.order = reinterpret_cast<int *>(wsb + w.order_off);
       sa.order = ta.order;
+      if (ta.hg && (long long)cache->L * cache->S * ta.ntiles < (1ll << 31))
+        ta.plan = reinterpret_cast<int *>(wsb + w.plan_off);
     }
   }
   if ((e = run_phases(cache, ta, stream)) != TRI_OK) return e;
