@@ -1125,7 +1125,7 @@ __global__ void __launch_bounds__(kThreads, 2) score_keys_mma_kernel(const __gri
 // slots' full barriers in turn, and a parity wait cannot match a phase two
 // back (a slot shared by both parities would let a warp that ran a cycle
 // ahead see the previous use's completed phase as its own).
-constexpr int kHgKeys = 4096;       // keys per CTA and head (one part entry)
+constexpr int kHgKeys = 8192;       // keys per CTA and head (one part entry)
 constexpr int kHgStages = 6;
 constexpr int kHgEarly = 4;         // stages issued before the weights are taken
 static_assert(kHgStages % 2 == 0, "ring slots must belong to one consumer parity");
